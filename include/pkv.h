@@ -1,0 +1,178 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache write and variable-length paged
+ * attention for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (the web pages the method comes from):
+ *   [page 1] "从 token 调度到采样输出，追踪每一步张量维度的变化，搞懂 LLM 推理到底在算什么"
+ *            (zizhi168.cn/news/2384056)
+ *   [page 2] "别只当API调用侠了！一文带你深入大模型“体内”，看懂推理全流程"
+ *            (su666666.com/news/35626)
+ *   [page 3] adg.csdn.net survey of LLM inference optimisation
+ *            (adg.csdn.net/695256bb5b9f5f31781b99f3)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *   never allocates device memory, never frees it, never synchronises the
+ *   stream and keeps no state between calls.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *   void*; NULL is the legacy default stream). A call returns as soon as the
+ *   kernels are queued.
+ * - bf16 tensors are raw 16-bit bfloat16 values. Layouts are row-major and
+ *   dense (no strides), with the shapes given beside each argument.
+ * - Host-detectable errors (null pointers, unsupported sizes, bad options)
+ *   return a non-zero pkv_status and enqueue nothing.
+ * - Device-detectable errors (an index that the tables give but that lies
+ *   outside the pool, inconsistent lengths) never trap: the offending item is
+ *   skipped, its outputs are unspecified, and the matching PKV_DEV_* bit is
+ *   OR-ed into *dev_status when dev_status is not NULL. The caller zeroes
+ *   *dev_status before the call and reads it after synchronising.
+ * - KV pool of one layer ([page 1] §02 gives the per-model pool
+ *   [num_layers, 2, num_blocks, block_size, num_kv_heads, head_dim]; a
+ *   multi-layer caller passes the base of one layer):
+ *       kv_pool [2][num_blocks][block_size][num_kv_heads][head_dim] bf16,
+ *       index 0 holds K, index 1 holds V; the pointer must be 16-byte aligned.
+ *   Supported: head_dim 64 or 128; block_size a multiple of 16 (up to 256);
+ *   num_heads a multiple of num_kv_heads.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pkv_status;
+
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG 1       /* null pointer, negative size, inconsistent shape */
+#define PKV_ERR_UNSUPPORTED 2       /* valid, but outside what the kernels implement */
+#define PKV_ERR_CUDA 3              /* a CUDA runtime call failed (e.g. launch) */
+#define PKV_ERR_WORKSPACE 4         /* workspace missing or smaller than required */
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_SLOT 1          /* slot_mapping entry outside [-1, num_blocks*block_size) */
+#define PKV_DEV_BAD_BLOCK 2         /* block_table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_LENGTHS 4       /* seq_len < query_len, cu_seqlens not monotone, or a
+                                       length beyond max_seq_len / max_query_len /
+                                       max_blocks_per_seq * block_size */
+#define PKV_DEV_TIMEOUT 8           /* an internal pipeline wait gave up; outputs of the
+                                       affected tile are unspecified */
+
+/*
+ * pkv_kv_cache_write -- scatter the step's new K/V rows into the paged pool.
+ * ([page 1] §02: slot_mapping says where each new K/V is written; a slot is
+ * physical_block * block_size + offset_in_block.)
+ *
+ *   kv_pool      [2][num_blocks][block_size][num_kv_heads][head_dim] bf16, in/out
+ *   k_new, v_new [num_tokens][num_kv_heads][head_dim] bf16 (16-byte aligned)
+ *   slot_mapping [num_tokens] int32; -1 skips the token (padding)
+ *
+ * For each token t with s = slot_mapping[t] >= 0:
+ *   kv_pool[0][s / block_size][s % block_size][:][:] = k_new[t]
+ *   kv_pool[1][s / block_size][s % block_size][:][:] = v_new[t]
+ * A bit copy; every other slot is left untouched. Slots must be distinct
+ * (duplicates race). num_tokens == 0 is a no-op.
+ * Errors: PKV_DEV_BAD_SLOT for a slot outside [-1, num_blocks*block_size).
+ */
+pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_new,
+                              const int32_t *slot_mapping, int32_t num_tokens,
+                              int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t *dev_status, void *stream);
+
+/*
+ * pkv_attention_workspace_size -- bytes of scratch that
+ * pkv_paged_attention_varlen needs for these sizes and this partition_size
+ * (0 when the call needs none). The caller allocates it (any 256-byte aligned
+ * device buffer at least this large) and may reuse it across calls on one
+ * stream; its contents need no initialisation.
+ */
+size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t max_seq_len, int32_t partition_size);
+
+/*
+ * pkv_paged_attention_varlen -- causal GQA attention of flattened queries
+ * over a paged KV cache.
+ * ([page 1] §03/§04: all requests' tokens are flattened into
+ * [num_sched_tokens] and separated by cu_seqlens; the six steps GQA-share,
+ * QK^T, scale, mask, softmax, times V; kv_head = q_head / (num_heads /
+ * num_kv_heads); block_table maps a request's logical blocks to physical
+ * ones ([page 2] PagedAttention deep-dive). [page 2] step 4: causal mask.
+ * [page 1] §07: long contexts are split and the pieces renormalised by
+ * log-sum-exp. [page 3] §3.4: the fused kernel is exact attention.)
+ *
+ *   out          [num_tokens][num_heads][head_dim] fp32, written
+ *   out_lse      [num_tokens][num_heads] fp32 natural-log log-sum-exp of the
+ *                scaled scores, written; may be NULL
+ *   q            [num_tokens][num_heads][head_dim] bf16 (16-byte aligned)
+ *   kv_pool      see above; the step's new K/V must already be written
+ *                (call pkv_kv_cache_write first, on the same stream)
+ *   block_table  [num_seqs][max_blocks_per_seq] int32 physical block ids
+ *   cu_seqlens_q [num_seqs + 1] int32, cu[0] = 0, cu[num_seqs] = num_tokens
+ *   seq_lens     [num_seqs] int32 context length of each request INCLUDING
+ *                its query_len = cu[i+1] - cu[i] new tokens
+ *   max_query_len, max_seq_len: upper bounds of the per-request values (the
+ *                host never reads device tables; the grid is sized by them)
+ *   scale        score scale, normally 1/sqrt(head_dim)
+ *   partition_size  split-KV partition length in tokens for query_len == 1
+ *                requests: 0 = never split, -1 = automatic (512), > 0 = a
+ *                multiple of 16
+ *   workspace, workspace_bytes: scratch of at least
+ *                pkv_attention_workspace_size(...) bytes (may be NULL when
+ *                that size is 0)
+ *
+ * Query j of request i sits at position pos = seq_len_i - query_len_i + j
+ * and attends to keys 0..pos (bottom-right causal alignment). Keys beyond
+ * seq_len_i are never read, so unwritten slots of a partial last block may
+ * hold anything, NaN included.
+ * Requests with query_len == 1 run on the decode kernel (CUDA cores,
+ * HBM-bound, split-KV + log-sum-exp merge when partitioned); requests with
+ * query_len > 1 run on the chunked-prefill kernel (tcgen05 tensor cores).
+ */
+pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
+                                      const void *kv_pool, const int32_t *block_table,
+                                      int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q,
+                                      const int32_t *seq_lens, int32_t num_seqs,
+                                      int32_t num_tokens, int32_t max_query_len,
+                                      int32_t max_seq_len, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks, float scale,
+                                      int32_t partition_size, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream);
+
+/*
+ * pkv_lse_merge -- combine partial attention results by log-sum-exp
+ * ([page 1] §07: chunked prefill, Flash-Decoding and sequence parallelism
+ * renormalise their pieces with log-sum-exp).
+ *
+ *   part_out [num_parts][num_tokens][num_heads][head_dim] fp32
+ *   part_lse [num_parts][num_tokens][num_heads] fp32
+ *   out      [num_tokens][num_heads][head_dim] fp32, written
+ *   out_lse  [num_tokens][num_heads] fp32, written; may be NULL
+ *
+ * Per row: M = max_p lse_p, w_p = exp(lse_p - M),
+ *   out = sum_p w_p * part_out_p / sum_p w_p,  lse = M + ln(sum_p w_p).
+ * A partition with lse = -inf is empty and its part_out is not read; a row
+ * whose partitions are all empty gives out = 0 and lse = -inf.
+ * head_dim must be a multiple of 4 (at most 512); pointers 16-byte aligned.
+ */
+pkv_status pkv_lse_merge(float *out, float *out_lse, const float *part_out,
+                         const float *part_lse, int32_t num_parts, int32_t num_tokens,
+                         int32_t num_heads, int32_t head_dim, void *stream);
+
+/* Human-readable name of a pkv_status value (static storage). */
+const char *pkv_status_string(pkv_status status);
+
+/* ABI version of this header: 1. */
+int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */
