@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-attention step on GB300.
+
+A step is the whole hot path over one batch: the KV write of the step's new
+K/V rows (slot_mapping) followed by varlen paged attention (decode kernel,
+split-KV log-sum-exp merge, chunked-prefill kernel as the batch needs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config llama3_8b_decode]
+
+Prints ONE JSON line (rank 0). ``value`` is KV GB/s (algorithmic bytes: every
+request reads its whole context once, 2*Hkv*D*2 bytes per token) over the
+device-resident step time; ``e2e`` repeats the measurement with the step's
+inputs copied from pinned host memory and the output copied back inside the
+timed region. ``--impl reference`` times the fp64 CPU oracle on the host
+cores instead (bounded sample of the same workload).
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
+(requests are independent, so the path shards with no collective); timing is
+the max over ranks, ``value`` the total bytes of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="llama3_8b_decode")
+    ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target length of the oracle CPU-baseline sample")
+    return ap.parse_args()
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "merge.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_varlen_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per attention launch from the committed ncu summary, or
+    None when the summary is missing or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", f"decode_{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_val = re.search(r"traffic_bytes_per_attention_call:\s*([0-9]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_val.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_step_seconds(w, budget_s: float):
+    """Time the oracle on whole steps of the workload (KV write + attention
+    of every request); repeat until about `budget_s` seconds of CPU time."""
+    import oracle as oracle_pkg
+
+    orc = oracle_pkg.load()
+    cores = orc.num_threads()
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        pool = orc.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
+        orc.paged_attention(w.q, pool, w.block_table, w.cu_seqlens, w.seq_lens, w.scale)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all >= budget_s or len(times) >= 50:
+            break
+    return statistics.median(times), cores, len(times)
+
+
+def oracle_sample(w, budget_s: float):
+    """A bounded sample of the workload for the oracle: the full batch when
+    one oracle step fits the budget, otherwise its first requests."""
+    from paged_kv_cache_varlen_gb300 import workloads as wl
+
+    work = int((w.seq_lens.astype(np.int64) * w.query_lens).sum())
+    if work <= 4_000_000:  # ~ a few seconds of fp64 work on a many-core host
+        return w, f"whole batch ({w.num_seqs} requests), repeated"
+    # keep requests in order until the key count reaches the cap
+    keep = np.searchsorted(np.cumsum(w.seq_lens.astype(np.int64) * w.query_lens), 4_000_000) + 1
+    keep = max(1, min(int(keep), w.num_seqs))
+    sub = wl.build(w.name + "_sample", w.seq_lens[:keep], w.query_lens[:keep], w.num_heads,
+                   w.num_kv_heads, w.head_dim, w.block_size, seed=w.seed, poison=False)
+    return sub, f"first {keep} of {w.num_seqs} requests, repeated"
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_varlen_gb300 import workloads as wl
+
+    w = wl.CONFIGS[args.config](poison=False)
+    sample, desc = oracle_sample(w, args.cpu_seconds)
+    steps_needed = max(1, args.steps)
+    sec, cores, n = oracle_step_seconds(sample, min(args.cpu_seconds, 60.0))
+    gbs = sample.kv_bytes() / sec / 1e9
+    line = {
+        "impl": "reference", "metric": "paged decode attention KV GB/s", "value": gbs,
+        "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": 0, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "seqs_per_s": sample.num_seqs / sec,
+        "config": {"workload": w.name, "requested_steps": steps_needed},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    from paged_kv_cache_varlen_gb300 import binding as pkv
+    from paged_kv_cache_varlen_gb300 import build as pkv_build
+    from paged_kv_cache_varlen_gb300 import workloads as wl
+
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    pkv_build.build()
+    pkv.load_library()
+
+    base = wl.CONFIGS[args.config]
+    seed_default = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4,
+                    "mixed_step": 5}[args.config]
+    w = base(seed=seed_default + 1000 * rank, poison=False)
+    T, H, D = w.q.shape
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = {
+        "q": bf16(w.q).pin_memory(), "k_new": bf16(w.k_new).pin_memory(),
+        "v_new": bf16(w.v_new).pin_memory(),
+        "slots": torch.from_numpy(w.slot_mapping).pin_memory(),
+        "table": torch.from_numpy(w.block_table).pin_memory(),
+        "cu": torch.from_numpy(w.cu_seqlens).pin_memory(),
+        "lens": torch.from_numpy(w.seq_lens).pin_memory(),
+    }
+    d = {k: v.to(dev) for k, v in host.items()}
+    pool = bf16(w.pool).to(dev)
+    out = torch.empty((T, H, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D, w.max_seq_len,
+                                            args.partition_size)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q, k_new, v_new, slots, table, cu, lens, ev=None):
+        pkv.kv_cache_write(pool, k_new, v_new, slots, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.paged_attention_varlen(q, pool, table, cu, lens, w.max_query_len, w.max_seq_len,
+                                   out=out, out_lse=lse, scale=w.scale,
+                                   partition_size=args.partition_size, workspace=ws,
+                                   stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    dev_args = (d["q"], d["k_new"], d["v_new"], d["slots"], d["table"], d["cu"], d["lens"])
+    for _ in range(max(3, args.warmup)):
+        step(*dev_args)
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region -------------------------------------
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for k in range(K):
+        step(*dev_args, ev=evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(stop)
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+
+    # ---- end-to-end: inputs from pinned host memory, output back -----------
+    E = args.e2e_steps if args.e2e_steps is not None else max(3, K // 4)
+    out_host = torch.empty((T, H, D), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(E):
+        for kname in host:
+            d[kname].copy_(host[kname], non_blocking=True)
+        step(*dev_args)
+        out_host.copy_(out, non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_stop)
+
+    # ---- reduce over ranks --------------------------------------------------
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = max_over_ranks(total_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    attn_avg_ms = max_over_ranks(attn_avg_ms)
+
+    kv_bytes = w.kv_bytes()
+    ms_per_step = total_ms / K
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms / E * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
+    nparts = 1 if args.partition_size == 0 else -(-w.max_seq_len // (args.partition_size
+                                                                       if args.partition_size > 0
+                                                                       else 512))
+    launches_per_step = 1 + 1 + (1 if nparts > 1 else 0) + (1 if w.max_query_len > 1 else 0)
+    cpu = None
+    if rank == 0 and world == 1:
+        sample, desc = oracle_sample(w, args.cpu_seconds)
+        sec, cores, n = oracle_step_seconds(sample, args.cpu_seconds)
+        cpu = {"value": sample.kv_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
+               "kind": "oracle", "sample": f"{desc}; {n} oracle steps, median",
+               "seqs_per_s": sample.num_seqs / sec}
+    if rank == 0:
+        line = {
+            "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
+            "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_heads": H,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": D,
+                       "block_size": w.block_size, "max_seq_len": w.max_seq_len,
+                       "kv_bytes_per_step": kv_bytes, "partition_size": args.partition_size,
+                       "l2": "inputs larger than L2 (KV read per step >> 126 MB L2), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "attention call (decode + split-KV merge)",
+                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profiled_traffic(args.config)},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": e2e_ms / E},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,236 @@
+// api.cpp -- the C ABI of libpkv (declared in include/pkv.h): host-side
+// argument validation, TMA tensor-map encoding and kernel dispatch.
+//
+// Nothing here allocates device memory, synchronises a stream or keeps
+// state across calls (the only cached item is the driver entry point of
+// cuTensorMapEncodeTiled and per-kernel shared-memory attributes).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "launch.h"
+
+namespace {
+
+using pkv::AttnParams;
+
+constexpr int32_t kAutoPartition = 512;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with byte strides s1, s2.
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+               CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Partition length and count for query_len == 1 requests.
+bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps, int32_t* np) {
+  if (partition_size < -1) return false;
+  if (partition_size > 0 && partition_size % 16 != 0) return false;
+  const int32_t len = max_seq_len > 0 ? max_seq_len : 1;
+  int32_t s = partition_size == 0 ? ((len + 15) / 16) * 16
+                                  : (partition_size < 0 ? kAutoPartition : partition_size);
+  int32_t n = (len + s - 1) / s;
+  if (n <= 1) {
+    n = 1;
+    if (s < len) s = ((len + 15) / 16) * 16;
+  }
+  *ps = s;
+  *np = n;
+  return true;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t workspace_bytes_for(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t nparts) {
+  if (nparts <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * nparts * num_heads;
+  return round_up(rows * head_dim * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t pkv_abi_version(void) { return 1; }
+
+pkv_status pkv_kv_cache_write(void* kv_pool, const void* k_new, const void* v_new,
+                              const int32_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                              int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!kv_pool || !k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(kv_pool) || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+  if (((int64_t)num_kv_heads * head_dim) % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  pkv::KvWriteParams p;
+  p.pool = kv_pool;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slot_mapping = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.num_slots = (int64_t)num_blocks * block_size;
+  p.row_vecs = num_kv_heads * head_dim / 8;
+  p.status = dev_status;
+  return pkv::launch_kv_write(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
+                                                                                    : PKV_ERR_CUDA;
+}
+
+size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len,
+                                    int32_t partition_size) {
+  (void)num_tokens;
+  (void)num_kv_heads;
+  int32_t ps = 0, np = 1;
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
+  if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return 0;
+  return workspace_bytes_for(num_seqs, num_heads, head_dim, np);
+}
+
+pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
+                                      const void* kv_pool, const int32_t* block_table,
+                                      int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                      const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t num_tokens, int32_t max_query_len,
+                                      int32_t max_seq_len, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int32_t num_blocks, float scale, int32_t partition_size,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (num_seqs == 0) return PKV_ERR_INVALID_ARG;
+  if (!out || !q || !kv_pool || !block_table || !cu_seqlens_q || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (max_query_len < 1 || max_seq_len < max_query_len) return PKV_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 || block_size > 256) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)2 * num_blocks * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int32_t group = num_heads / num_kv_heads;
+  if (max_query_len > 1 && (group > 128 || (128 % group) != 0)) return PKV_ERR_UNSUPPORTED;
+
+  int32_t ps = 0, np = 1;
+  if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
+  const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, np);
+  if (need > 0 && (!workspace || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return PKV_ERR_WORKSPACE;
+
+  AttnParams p;
+  p.out = out;
+  p.out_lse = out_lse;
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.cu_seqlens = cu_seqlens_q;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.max_query_len = max_query_len;
+  p.max_seq_len = max_seq_len;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.part_size = ps;
+  p.num_parts = np;
+  p.ws_out = nullptr;
+  p.ws_lse = nullptr;
+  if (need > 0) {
+    const size_t rows = (size_t)num_seqs * np * num_heads;
+    p.ws_out = static_cast<float*>(workspace);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round_up(rows * head_dim * sizeof(float), 256));
+  }
+  p.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const uint64_t D = (uint64_t)head_dim;
+  const uint64_t pool_rows = (uint64_t)2 * num_blocks * block_size;
+  // decode: a 16-key box of whole rows, no swizzle
+  CUtensorMap kv_rows;
+  if (!encode_3d(&kv_rows, kv_pool, D, num_kv_heads, pool_rows, D * 2, (uint64_t)num_kv_heads * D * 2,
+                 (uint32_t)D, 1, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return PKV_ERR_CUDA;
+  if (pkv::launch_decode(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (np > 1 && pkv::launch_decode_merge(p, st) != cudaSuccess) return PKV_ERR_CUDA;
+
+  if (max_query_len > 1) {
+    CUtensorMap q_map, kv_sw;
+    if (!encode_3d(&q_map, q, D, num_heads, num_tokens, D * 2, (uint64_t)num_heads * D * 2, 64,
+                   (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    if (!encode_3d(&kv_sw, kv_pool, D, num_kv_heads, pool_rows, D * 2,
+                   (uint64_t)num_kv_heads * D * 2, 64, 1, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    if (pkv::launch_prefill(p, q_map, kv_sw, st) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_lse_merge(float* out, float* out_lse, const float* part_out, const float* part_lse,
+                         int32_t num_parts, int32_t num_tokens, int32_t num_heads,
+                         int32_t head_dim, void* stream) {
+  if (num_parts < 1 || num_tokens < 0 || num_heads < 1 || head_dim < 1) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!out || !part_out || !part_lse) return PKV_ERR_INVALID_ARG;
+  if (head_dim % 4 != 0 || head_dim > 512) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(out) || !aligned16(part_out)) return PKV_ERR_INVALID_ARG;
+  return pkv::launch_lse_merge(out, out_lse, part_out, part_lse, num_parts,
+                               (int64_t)num_tokens * num_heads, head_dim,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

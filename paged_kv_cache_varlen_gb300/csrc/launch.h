@@ -1,0 +1,68 @@
+// launch.h -- internal launch interface between the C-ABI layer (api.cpp)
+// and the kernels. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; no driver-API linkage)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct KvWriteParams {
+  void* pool;                 // [2][NB][BS][Hkv][D] bf16
+  const void* k_new;          // [T][Hkv][D] bf16
+  const void* v_new;          // [T][Hkv][D] bf16
+  const int32_t* slot_mapping;  // [T]
+  int32_t num_tokens;
+  int64_t num_slots;          // NB * BS
+  int32_t row_vecs;           // 16-byte vectors per token row = Hkv * D / 8
+  int32_t* status;
+};
+
+// Attention problem shared by the decode, merge and prefill kernels.
+struct AttnParams {
+  float* out;                 // [T][H][D] fp32
+  float* out_lse;             // [T][H] fp32 or null
+  const uint16_t* q;          // [T][H][D] bf16
+  const int32_t* block_table; // [B][max_blocks]
+  const int32_t* cu_seqlens;  // [B+1]
+  const int32_t* seq_lens;    // [B]
+  int32_t max_blocks;
+  int32_t num_seqs, num_tokens, max_query_len, max_seq_len;
+  int32_t num_heads, num_kv_heads, head_dim, block_size, num_blocks;
+  float scale_log2;           // scale * log2(e)
+  // split-KV for query_len == 1 requests
+  int32_t part_size;          // tokens per partition (multiple of 16)
+  int32_t num_parts;          // partitions per request covering max_seq_len
+  float* ws_out;              // [B][num_parts][H][D] (null when num_parts == 1)
+  float* ws_lse;              // [B][num_parts][H]
+  int32_t* status;
+};
+
+cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
+
+// Decode kernel (query_len == 1 requests), CUDA cores, TMA-staged pages.
+// `kv_map` views the pool as [2*NB*BS rows][Hkv][D] with a box of
+// {D, 1, 16}.
+cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream);
+
+// Log-sum-exp merge of the decode kernel's partitions (requests whose
+// context spans more than one partition).
+cudaError_t launch_decode_merge(const AttnParams& p, cudaStream_t stream);
+
+// Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
+// `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle;
+// `kv_map`: pool rows with a box of {64, 1, 16}, 128-byte swizzle.
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
+                           const CUtensorMap& kv_map, cudaStream_t stream);
+
+// Public dense merge: part_out [P][T*H][D], part_lse [P][T*H].
+cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,
+                             const float* part_lse, int32_t num_parts, int64_t num_rows,
+                             int32_t head_dim, cudaStream_t stream);
+
+// Shared-memory bytes a prefill CTA needs for this head_dim (for validation).
+size_t prefill_smem_bytes(int head_dim);
+size_t decode_smem_bytes(int head_dim);
+
+}  // namespace pkv

@@ -1,0 +1,124 @@
+"""The C ABI library: it loads, exports every symbol ``include/pkv.h``
+declares, and its host-side checks reject bad arguments before touching the
+GPU (CPU only: no kernel runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_varlen_gb300 import binding, build
+
+    build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("pkv_kv_cache_write", "pkv_paged_attention_varlen", "pkv_lse_merge",
+              "pkv_attention_workspace_size", "pkv_status_string", "pkv_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(4).startswith(b"workspace")
+
+
+def test_workspace_size_arithmetic(lib):
+    # one partition: nothing to merge, no workspace
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 512, -1) == 0
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 0) == 0
+    # 4096 / 512 = 8 partitions: [B][8][H][D] fp32 + [B][8][H] fp32, 256-byte aligned pieces
+    rows = 64 * 8 * 32
+    expect = -(-rows * 128 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, -1) == expect
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 512) == expect
+    # explicit partition must be a multiple of 16
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 100) == 0
+
+
+def _attn(lib, **over):
+    args = dict(out=16, out_lse=None, q=16, kv_pool=16, block_table=16, max_blocks=4, cu=16,
+                seq_lens=16, num_seqs=1, num_tokens=1, max_query_len=1, max_seq_len=16,
+                num_heads=4, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=4,
+                scale=0.125, partition_size=-1, workspace=None, workspace_bytes=0,
+                dev_status=None, stream=None)
+    args.update(over)
+    return lib.pkv_paged_attention_varlen(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"num_tokens": -1}, 1),
+    ({"num_seqs": 0}, 1),
+    ({"out": None}, 1),
+    ({"q": None}, 1),
+    ({"num_heads": 6, "num_kv_heads": 4}, 1),
+    ({"max_query_len": 0}, 1),
+    ({"max_seq_len": 0}, 1),
+    ({"scale": 0.0}, 1),
+    ({"scale": float("nan")}, 1),
+    ({"q": 24}, 1),                      # not 16-byte aligned
+    ({"head_dim": 96}, 2),
+    ({"block_size": 8}, 2),
+    ({"block_size": 512}, 2),
+    ({"max_query_len": 2, "num_heads": 6, "num_kv_heads": 2}, 2),   # group 3 on the MMA path
+    ({"partition_size": 100}, 1),
+    ({"partition_size": -2}, 1),
+    ({"max_seq_len": 4096, "partition_size": 512}, 4),             # needs workspace
+])
+def test_attention_rejects_before_launch(lib, over, status):
+    assert _attn(lib, **over) == status
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _attn(lib, num_tokens=0, out=None, q=None) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, 16, 16, 16, -1, 4, 16, 2, 128, None, None), 1),
+    ((None, 16, 16, 16, 3, 4, 16, 2, 128, None, None), 1),
+    ((16, 16, 16, 16, 3, 0, 16, 2, 128, None, None), 1),
+    ((16, 16, 24, 16, 3, 4, 16, 2, 128, None, None), 1),
+    ((16, 16, 16, 16, 3, 4, 16, 1, 4, None, None), 2),
+    ((16, 16, 16, 16, 0, 4, 16, 2, 128, None, None), 0),
+])
+def test_kv_write_rejects_before_launch(lib, args, status):
+    assert lib.pkv_kv_cache_write(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, None, 16, 16, 0, 4, 2, 128, None), 1),
+    ((16, None, 16, 16, 2, 4, 2, 130, None), 2),
+    ((16, None, 16, 16, 2, 4, 2, 1024, None), 2),
+    ((None, None, 16, 16, 2, 4, 2, 128, None), 1),
+    ((16, None, 16, 16, 2, 0, 2, 128, None), 0),
+])
+def test_lse_merge_rejects_before_launch(lib, args, status):
+    assert lib.pkv_lse_merge(*args) == status
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from paged_kv_cache_varlen_gb300 import binding
+
+    with pytest.raises(binding.PkvError):
+        binding.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,217 @@
+"""GPU edge cases (needs a GB300): split-KV partition sizes, ragged tails,
+GQA group sizes, head_dim 64, larger blocks, short query chunks, the
+invariants the oracle is pinned to (block permutation, copy-on-write
+aliasing, length-1 contexts), device-side error bits and the public
+log-sum-exp merge."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_varlen_gb300 import binding as pkv
+from paged_kv_cache_varlen_gb300 import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _run_and_check(oracle, w, partition_size=-1, rows=None):
+    ref_pool = oracle.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    out, lse = dev.attend(partition_size=partition_size)
+    assert dev.dev_status() == 0
+    ref_o, ref_l = oracle.paged_attention(w.q, ref_pool, w.block_table, w.cu_seqlens, w.seq_lens,
+                                          w.scale, rows=rows)
+    gu.compare(out, lse, ref_o, ref_l, rows=rows)
+    return dev, out, lse
+
+
+@pytest.mark.parametrize("partition_size", [0, 16, 48, 128, 512, 2048, -1])
+def test_decode_partition_sizes(oracle, partition_size):
+    w = wl.build("parts", [1, 15, 16, 17, 511, 512, 513, 1500, 3001], [1] * 9, 32, 8, 128,
+                 seed=201)
+    _run_and_check(oracle, w, partition_size)
+
+
+def test_one_partition_equals_no_split_bitwise():
+    w = wl.build("onepart", [100, 700, 1023], [1, 1, 1], 32, 8, 128, seed=202)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    a = dev.attend(partition_size=0)
+    b = dev.attend(partition_size=1024)   # every context fits one partition
+    assert dev.dev_status() == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("H,Hkv", [(32, 8), (8, 8), (32, 32), (32, 1), (16, 8), (64, 8), (4, 2)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_group_sizes_and_head_dims_decode(oracle, H, Hkv, D):
+    w = wl.build("gqa", [1, 33, 300, 1111], [1, 1, 1, 1], H, Hkv, D, seed=203 + H + Hkv + D)
+    _run_and_check(oracle, w, 256)
+
+
+@pytest.mark.parametrize("H,Hkv", [(32, 8), (8, 8), (32, 1), (16, 8), (8, 2)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_group_sizes_and_head_dims_prefill(oracle, H, Hkv, D):
+    w = wl.build("gqa_pre", [300, 40, 1, 257], [200, 40, 1, 17], H, Hkv, D, seed=204 + H + D)
+    _run_and_check(oracle, w)
+
+
+@pytest.mark.parametrize("BS", [16, 32, 64, 256])
+def test_block_sizes(oracle, BS):
+    w = wl.build("bs", [5, 77, 400, 1030], [1, 1, 70, 3], 32, 8, 128, block_size=BS, seed=205 + BS)
+    _run_and_check(oracle, w, 128)
+
+
+@pytest.mark.parametrize("qlens", [[2, 3, 4, 5, 6, 7, 8, 2], [33, 31, 1, 64, 65, 127, 129, 2]])
+def test_short_query_chunks(oracle, qlens):
+    """Speculative-verify sized chunks and chunk lengths around the 32-query
+    tile, each over a cached prior context, mixed with decodes."""
+    prior = [0, 5, 16, 100, 1000, 17, 4095, 64]
+    L = [p + q for p, q in zip(prior, qlens)]
+    w = wl.build("short", L, qlens, 32, 8, 128, seed=206 + sum(qlens))
+    _run_and_check(oracle, w)
+
+
+def test_full_prefill_without_prior_context(oracle):
+    w = wl.build("fresh", [1, 2, 127, 128, 129, 600], [1, 2, 127, 128, 129, 600], 32, 8, 128,
+                 seed=207)
+    _run_and_check(oracle, w)
+
+
+def test_length_one_context_returns_v_exactly():
+    w = wl.build("l1", [1, 1, 1], [1, 1, 1], 32, 8, 128, seed=208)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    out, _ = dev.attend()
+    assert dev.dev_status() == 0
+    G = 4
+    v = wl.bf16_bits_to_f32(w.v_new)
+    ref = np.repeat(v, G, axis=1)          # head h reads kv head h // G
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("qlen", [1, 300])
+def test_block_permutation_is_bitwise_invisible(qlen):
+    w = wl.build("perm", [1400, 333], [1, qlen], 32, 8, 128, seed=209, pool_factor=1.5)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    out, lse = dev.attend()
+    perm = np.random.default_rng(210).permutation(w.num_blocks)
+    perm_t = torch.from_numpy(perm).cuda()
+    pool2 = torch.empty_like(dev.pool)
+    pool2[:, perm_t] = dev.pool
+    bt2 = np.where(w.block_table >= 0, perm[np.maximum(w.block_table, 0)], -1)
+    out2, lse2 = dev.attend(pool=pool2, table=gu.i32_tensor(bt2))
+    assert dev.dev_status() == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_copy_on_write_aliasing_is_bitwise_invisible():
+    """The page's copy-on-write example: requests A = [7, 2] and B = [7, 6, 4]
+    share physical block 7; a private copy of it for B changes nothing."""
+    with open(os.path.join(GOLDEN, "block_tables.json")) as f:
+        g = json.load(f)
+    a_tab, b_tab = g["cow_request_a"], g["cow_request_b"]
+    BS, H, Hkv, D, NB = 16, 32, 8, 128, 12
+    rng = np.random.default_rng(211)
+    pool = wl.to_bf16_bits(rng.standard_normal((2, NB, BS, Hkv, D), dtype=np.float32))
+    q = wl.to_bf16_bits(rng.standard_normal((2, H, D), dtype=np.float32))
+    lens = np.array([2 * BS, 3 * BS - 5], np.int32)
+    cu = np.array([0, 1, 2], np.int32)
+
+    def run(pool_np, table):
+        out = torch.empty((2, H, D), dtype=torch.float32, device="cuda")
+        lse = torch.empty((2, H), dtype=torch.float32, device="cuda")
+        pkv.paged_attention_varlen(gu.bf16_tensor(q), gu.bf16_tensor(pool_np),
+                                   gu.i32_tensor(np.array(table, np.int32)), gu.i32_tensor(cu),
+                                   gu.i32_tensor(lens), 1, int(lens.max()), out=out, out_lse=lse)
+        return out, lse
+
+    o1, l1 = run(pool, [a_tab + [-1], b_tab])
+    pool2 = pool.copy()
+    pool2[:, 9] = pool[:, g["shared_physical_block"]]
+    o2, l2 = run(pool2, [a_tab + [-1], [9] + b_tab[1:]])
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_nan_poisoned_free_slots_never_leak(oracle):
+    """Unwritten slots of every partial last block hold bf16 NaN (the
+    workload generator poisons them); outputs must stay finite and exact."""
+    w = wl.build("nan", [17, 31, 130, 260], [1, 20, 130, 3], 32, 8, 128, seed=212)
+    assert np.any(w.pool == wl.BF16_NAN)
+    _run_and_check(oracle, w)
+
+
+def test_empty_batch_is_a_no_op():
+    out = torch.full((0, 32, 128), 1.0, device="cuda")
+    q = torch.zeros((0, 32, 128), dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros((2, 4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    cu = torch.zeros(2, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_attention_varlen(q, pool, bt, cu, lens, 1, 1, out=out)
+    slots = torch.zeros(0, dtype=torch.int32, device="cuda")
+    kn = torch.zeros((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    pkv.kv_cache_write(pool, kn, kn, slots)
+    torch.cuda.synchronize()
+
+
+def test_device_errors_set_status_bits_and_spare_other_requests(oracle):
+    w = wl.build("bad", [40, 300, 50], [1, 1, 20], 32, 8, 128, seed=213)
+    ref_pool = oracle.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
+    ref_o, _ = oracle.paged_attention(w.q, ref_pool, w.block_table, w.cu_seqlens, w.seq_lens,
+                                      w.scale)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    assert dev.dev_status() == 0
+    # a block id outside the pool in request 1 (decode) and request 2 (prefill)
+    bad = w.block_table.copy()
+    bad[1, 3] = w.num_blocks + 5
+    bad[2, 1] = -7
+    out, _ = dev.attend(table=gu.i32_tensor(bad))
+    assert dev.dev_status() & gu.pkv.DEV_BAD_BLOCK
+    got = out.cpu().numpy()
+    assert np.max(np.abs(got[0] - ref_o[0])) <= gu.ATOL   # request 0 untouched
+    # a context shorter than its query chunk
+    dev.status.zero_()
+    lens = w.seq_lens.copy()
+    lens[2] = 5
+    dev.attend(lens=gu.i32_tensor(lens))
+    assert dev.dev_status() & gu.pkv.DEV_BAD_LENGTHS
+    # a slot outside the pool
+    dev.status.zero_()
+    slots = w.slot_mapping.copy()
+    slots[0] = w.num_blocks * w.block_size + 3
+    pkv.kv_cache_write(dev.pool, dev.k_new, dev.v_new, gu.i32_tensor(slots),
+                       dev_status=dev.status)
+    assert dev.dev_status() & gu.pkv.DEV_BAD_SLOT
+
+
+@pytest.mark.parametrize("P,T,H,D", [(1, 3, 4, 128), (5, 7, 32, 128), (64, 2, 8, 64),
+                                     (3, 4, 2, 256), (2, 1, 1, 4)])
+def test_public_lse_merge(oracle, P, T, H, D):
+    rng = np.random.default_rng(214 + P + D)
+    po = rng.standard_normal((P, T, H, D)).astype(np.float32)
+    pl = (rng.standard_normal((P, T, H)) * 3).astype(np.float32)
+    if P > 1:
+        pl[0, 0] = -np.inf          # an empty partition
+        po[0, 0] = np.nan           # ... whose output must not be read
+        pl[:, -1, -1] = -np.inf     # a row with no keys at all
+    ref_o, ref_l = oracle.lse_merge(po.astype(np.float64), pl.astype(np.float64))
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    out, _ = pkv.lse_merge(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(), out_lse=lse)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    l = lse.cpu().numpy()
+    assert np.all(np.isfinite(o))
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(l), fin)
+    assert np.max(np.abs(o - ref_o)) <= 1e-5
+    assert np.max(np.abs(l[fin] - ref_l[fin])) <= 1e-5
