@@ -291,6 +291,7 @@ def run_ours(args):
 
     # ---- end-to-end: inputs from pinned host memory, output back -----------
     E = args.e2e_steps if args.e2e_steps is not None else max(3, K // 4)
+    E = max(E, 1)
     out_host = torch.empty((T, H, D), dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -331,7 +332,7 @@ def run_ours(args):
                                                                        else 512))
     launches_per_step = 1 + 1 + (1 if nparts > 1 else 0) + (1 if w.max_query_len > 1 else 0)
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         sample, desc = oracle_sample(w, args.cpu_seconds)
         sec, cores, n = oracle_step_seconds(sample, args.cpu_seconds)
         cpu = {"value": sample.kv_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,

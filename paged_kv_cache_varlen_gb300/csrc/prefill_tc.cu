@@ -19,12 +19,16 @@
 //     physical block comes from block_table (no multicast);
 //   * S = Q K^T (M=128, N=128, K=head_dim) and O += P V (M=128, N=head_dim,
 //     K=128) run as tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued
-//     by one thread; S (double-buffered), P (double-buffered, bf16) and O
-//     live in tensor memory; P is the A operand straight from TMEM;
+//     by one thread; S (double-buffered), P and O live in tensor memory; P
+//     is the A operand straight from TMEM. P is split into a bf16 high part
+//     and a bf16 remainder, P ~= hi + lo to ~2^-16 relative, and O
+//     accumulates hi*V + lo*V: a single bf16 rounding of P alone (2^-9
+//     relative) puts few-key rows up to ~4e-3 off the exact result;
 //   * four softmax warps own one TMEM lane (= one Q row) per thread: they
 //     read S with tcgen05.ld, apply the causal mask and the online softmax
 //     (exp2 domain, lazy rescale when the maximum grows by more than 8),
-//     write P with tcgen05.st and rescale O in TMEM when needed;
+//     write P (hi and lo) with tcgen05.st once the previous tile's PV is
+//     done, and rescale O in TMEM when needed;
 //   * warp 4 produces TMA loads into a 2-stage K/V ring, warp 5 issues the
 //     MMAs; QK^T of tile j+1 overlaps the softmax of tile j;
 //   * every wait is bounded; on a timeout the CTA drains its copies and
@@ -61,7 +65,8 @@ struct PrefillLayout {
   // TMEM columns
   __device__ static constexpr uint32_t s_col(int b) { return 128u * (uint32_t)b; }
   static constexpr uint32_t O_COL = 256;
-  __device__ static constexpr uint32_t p_col(int b) { return 256u + D + 64u * (uint32_t)b; }
+  static constexpr uint32_t P_HI_COL = 256 + D;       // bf16(P), 64 columns
+  static constexpr uint32_t P_LO_COL = 256 + D + 64;  // bf16(P - bf16(P)), 64 columns
 };
 
 struct Bars {
@@ -267,8 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(tmem + Lay::O_COL, tmem + Lay::p_col(j & 1) + kk * 8, b, idesc_pv,
+          umma_ts(tmem + Lay::O_COL, tmem + Lay::P_HI_COL + kk * 8, b, idesc_pv,
                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
+          umma_ts(tmem + Lay::O_COL, tmem + Lay::P_LO_COL + kk * 8, b, idesc_pv, 1u);
         }
         umma_commit(smem_addr(&bars->kv_empty[j % kNS]));
         umma_commit(smem_addr(&bars->o_done));
@@ -326,19 +336,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mnew;
       }
       float rs = 0.f;
-      uint32_t pk[kBN / 2];
+      uint32_t pk[kBN / 2], pl[kBN / 2];
 #pragma unroll
       for (int c = 0; c < kBN / 2; ++c) {
         const float p0 = fast_exp2(fmaf(f[2 * c], sl2, -m));
         const float p1 = fast_exp2(fmaf(f[2 * c + 1], sl2, -m));
         rs += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
+        pl[c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
       }
       l = l * alpha + rs;
+      if (j > 0) {
+        // PV of the previous tile must be done: it reads the P buffer we are
+        // about to overwrite, and it writes the O we may rescale below.
+        ok = __all_sync(full, mbar_wait(smem_addr(&bars->o_done), (j - 1) & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
       {
-        const uint32_t pa = tmem + lane_base + Lay::p_col(j & 1);
-        PKV_TMEM_ST32(pa + 0, (pk + 0));
-        PKV_TMEM_ST32(pa + 32, (pk + 32));
+        const uint32_t ph = tmem + lane_base + Lay::P_HI_COL;
+        const uint32_t plo = tmem + lane_base + Lay::P_LO_COL;
+        PKV_TMEM_ST32(ph + 0, (pk + 0));
+        PKV_TMEM_ST32(ph + 32, (pk + 32));
+        PKV_TMEM_ST32(plo + 0, (pl + 0));
+        PKV_TMEM_ST32(plo + 32, (pl + 32));
         tmem_wait_st();
       }
       if (j == n_tiles - 1 && (kv_end % kBN) != 0) {
@@ -358,9 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       if (j > 0) {
-        ok = __all_sync(full, mbar_wait(smem_addr(&bars->o_done), (j - 1) & 1, p.status, abort));
-        if (!ok) break;
-        tc_fence_after();
         if (__any_sync(full, resc)) {
           const uint32_t oa = tmem + lane_base + Lay::O_COL;
 #pragma unroll

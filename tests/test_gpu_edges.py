@@ -214,4 +214,5 @@ def test_public_lse_merge(oracle, P, T, H, D):
     fin = np.isfinite(ref_l)
     assert np.array_equal(np.isfinite(l), fin)
     assert np.max(np.abs(o - ref_o)) <= 1e-5
-    assert np.max(np.abs(l[fin] - ref_l[fin])) <= 1e-5
+    if fin.any():
+        assert np.max(np.abs(l[fin] - ref_l[fin])) <= 1e-5
