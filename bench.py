@@ -243,7 +243,7 @@ def run_ours(args):
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D, w.max_seq_len,
                                             args.partition_size)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(q, k_new, v_new, slots, table, cu, lens, ev=None):

@@ -86,9 +86,13 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
 /*
  * pkv_attention_workspace_size -- bytes of scratch that
  * pkv_paged_attention_varlen needs for these sizes and this partition_size
- * (0 when the call needs none). The caller allocates it (any 256-byte aligned
- * device buffer at least this large) and may reuse it across calls on one
- * stream; its contents need no initialisation.
+ * (0 when the call needs none). The caller allocates it (a 256-byte aligned
+ * device buffer at least this large) and ZERO-FILLS it once before its first
+ * use (it holds per-request arrival counters of the split-KV merge). Every
+ * call that completes without PKV_DEV_TIMEOUT leaves it zero-filled again,
+ * so one workspace serves any number of calls on one stream; calls that may
+ * run concurrently need separate workspaces. After a PKV_DEV_TIMEOUT, clear
+ * it again before reuse.
  */
 size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
                                     int32_t num_kv_heads, int32_t head_dim,
@@ -119,8 +123,10 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  *                host never reads device tables; the grid is sized by them)
  *   scale        score scale, normally 1/sqrt(head_dim)
  *   partition_size  split-KV partition length in tokens for query_len == 1
- *                requests: 0 = never split, -1 = automatic (512), > 0 = a
- *                multiple of 16
+ *                requests: 0 = never split; -1 = automatic (512 tokens,
+ *                doubled until no request has more than 64 partitions);
+ *                > 0 = that many tokens, a multiple of 16. A split request's
+ *                partitions are merged by log-sum-exp inside the same kernel
  *   workspace, workspace_bytes: scratch of at least
  *                pkv_attention_workspace_size(...) bytes (may be NULL when
  *                that size is 0)
@@ -132,6 +138,9 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  * Requests with query_len == 1 run on the decode kernel (CUDA cores,
  * HBM-bound, split-KV + log-sum-exp merge when partitioned); requests with
  * query_len > 1 run on the chunked-prefill kernel (tcgen05 tensor cores).
+ * The kernels use programmatic dependent launch: each waits for the grid
+ * before it in the stream to finish before touching memory, so ordinary
+ * stream order holds.
  */
 pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
                                       const void *kv_pool, const int32_t *block_table,

@@ -142,7 +142,8 @@ def paged_attention_varlen(q: torch.Tensor, kv_pool: torch.Tensor, block_table: 
 
     Returns ``(out, out_lse)``; ``out`` is fp32 [T,H,D], ``out_lse`` fp32
     [T,H] or None. Missing ``out`` / ``workspace`` buffers are allocated with
-    torch (the library itself never allocates).
+    torch (the library itself never allocates); a workspace passed in must
+    have been zero-filled before its first use (``attention_workspace_size``).
     """
     _need(q, torch.bfloat16, 3, "q")
     _need(kv_pool, torch.bfloat16, 5, "kv_pool")
@@ -167,7 +168,7 @@ def paged_attention_varlen(q: torch.Tensor, kv_pool: torch.Tensor, block_table: 
         scale = 1.0 / math.sqrt(d)
     need = attention_workspace_size(b, t, h, hkv, d, max_seq_len, partition_size)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load_library().pkv_paged_attention_varlen(
         _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), _ptr(block_table),

@@ -20,6 +20,7 @@ namespace {
 using pkv::AttnParams;
 
 constexpr int32_t kAutoPartition = 512;
+constexpr int32_t kMaxAutoParts = 64;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -59,6 +60,9 @@ bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps,
   const int32_t len = max_seq_len > 0 ? max_seq_len : 1;
   int32_t s = partition_size == 0 ? ((len + 15) / 16) * 16
                                   : (partition_size < 0 ? kAutoPartition : partition_size);
+  // automatic: 512-token partitions, doubled until at most kMaxAutoParts per
+  // request (bounds the partials the in-kernel merge reads)
+  while (partition_size < 0 && (len + s - 1) / s > kMaxAutoParts) s *= 2;
   int32_t n = (len + s - 1) / s;
   if (n <= 1) {
     n = 1;
@@ -71,10 +75,21 @@ bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps,
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t workspace_bytes_for(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t nparts) {
-  if (nparts <= 1) return 0;
+// Workspace: partial outputs [B][P][H][D] fp32, partial lse [B][P][H] fp32,
+// arrival counters [B][H] int32 (zero between calls).
+struct WorkspaceLayout {
+  size_t lse_off, cnt_off, total;
+};
+
+WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                 int32_t nparts) {
+  WorkspaceLayout w{0, 0, 0};
+  if (nparts <= 1) return w;
   const size_t rows = (size_t)num_seqs * nparts * num_heads;
-  return round_up(rows * head_dim * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+  w.lse_off = round_up(rows * head_dim * sizeof(float), 256);
+  w.cnt_off = w.lse_off + round_up(rows * sizeof(float), 256);
+  w.total = w.cnt_off + round_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+  return w;
 }
 
 }  // namespace
@@ -125,7 +140,7 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
   int32_t ps = 0, np = 1;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return 0;
-  return workspace_bytes_for(num_seqs, num_heads, head_dim, np);
+  return workspace_layout(num_seqs, num_heads, head_dim, np).total;
 }
 
 pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
@@ -159,7 +174,8 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
 
   int32_t ps = 0, np = 1;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
-  const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, np);
+  const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, np);
+  const size_t need = wl.total;
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return PKV_ERR_WORKSPACE;
@@ -186,11 +202,11 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.num_parts = np;
   p.ws_out = nullptr;
   p.ws_lse = nullptr;
+  p.ws_cnt = nullptr;
   if (need > 0) {
-    const size_t rows = (size_t)num_seqs * np * num_heads;
     p.ws_out = static_cast<float*>(workspace);
-    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        round_up(rows * head_dim * sizeof(float), 256));
+    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_off);
+    p.ws_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.cnt_off);
   }
   p.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -203,7 +219,6 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
                  (uint32_t)D, 1, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return PKV_ERR_CUDA;
   if (pkv::launch_decode(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
-  if (np > 1 && pkv::launch_decode_merge(p, st) != cudaSuccess) return PKV_ERR_CUDA;
 
   if (max_query_len > 1) {
     CUtensorMap q_map, kv_sw;

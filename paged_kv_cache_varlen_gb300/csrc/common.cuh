@@ -148,6 +148,18 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the
+// stream has completed and its memory is visible; then allow the next grid
+// to be scheduled. Every kernel here calls both at its start, before it
+// reads or writes anything, so completion of a kernel still implies
+// completion of everything before it in the stream.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tcgen05) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -11,7 +11,7 @@
 //   page 3 §3.4: fused, exact attention (online softmax; scores never
 //     leave the SM).
 //   page 1 §07: a long context is split into partitions whose partial
-//     results are renormalised by log-sum-exp (merge.cu).
+//     results are renormalised by log-sum-exp.
 //
 // GB300 design:
 //   * one CTA = (request, KV head, head subgroup, partition); the CTA holds
@@ -22,19 +22,27 @@
 //     row stride of Hkv*D*2 bytes in the pool), fetched by one TMA tile
 //     load each into shared memory and completed on the slot's mbarrier.
 //     Warp w processes chunks w, w+4, w+8, ... and refills a slot as soon as
-//     it has consumed it, so up to 4*SPW chunks are in flight per CTA;
+//     it has consumed it;
 //   * inside a warp, LPT lanes cooperate on one token: each lane holds
 //     64/HG elements of every query head of the group (pre-scaled by
-//     scale*log2 e) and of the output accumulators, computes partial dot
-//     products with 16-byte shared-memory loads, and the lanes of the token
-//     reduce them with xor shuffles;
+//     scale*log2 e) and of the output accumulators, as float pairs for the
+//     packed fp32x2 FMA; the LPT partial dot products are reduced by a
+//     transpose-reduce over xor shuffles that leaves each lane with the full
+//     score of ONE head, so each lane runs the online softmax of one head
+//     and the probabilities are broadcast back for P*V;
 //   * online softmax in the exp2 domain with lazy rescaling: the running
 //     maximum only moves when a score exceeds it by more than 8 (a factor
 //     256), which keeps the rescale off the common path and is exact up to
-//     rounding;
+//     rounding; chunks whose 16 tokens are all valid take a check-free path;
 //   * the lane groups of a warp merge by shuffles, the warps through shared
-//     memory; the CTA writes the normalised output row (single partition)
-//     or the partition's normalised partial and its log-sum-exp (split).
+//     memory; a single-partition request is written directly. A split
+//     request writes its normalised partial and log-sum-exp to the
+//     workspace, and the last partition CTA to finish (an atomic counter per
+//     (request, head group), reset by that CTA) merges all partials by
+//     log-sum-exp -- no second kernel launch;
+//   * programmatic dependent launch: the kernel may start while the KV
+//     write that precedes it is finishing; it waits for that grid before
+//     reading anything, then lets the next kernel launch.
 #include <math.h>
 
 #include "common.cuh"
@@ -46,6 +54,7 @@ namespace {
 constexpr int kChunk = 16;  // tokens per TMA box and per pipeline stage
 constexpr int kWarps = 4;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int HG>
 struct DecodeGeometry {
@@ -56,18 +65,150 @@ struct DecodeGeometry {
   static constexpr int NPASS = (kChunk + TPW - 1) / TPW;
   static constexpr int ROW = D * 2;        // bytes of one K or V row
   static constexpr int SLOT = 2 * kChunk * ROW;
-  static_assert(LPT >= 1 && LPT <= 32 && (32 % LPT) == 0, "bad lanes per token");
+  static constexpr int LOG_HG = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
+  static_assert(LPT >= HG && LPT <= 32 && (32 % LPT) == 0, "bad lanes per token");
   static_assert(CPL >= 1, "at least one 16-byte vector per lane");
 };
 
-template <int D, int HG, int SPW>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(bf16_lo(w), bf16_hi(w));
+}
+
+// Reduce the HG partial dot products v[] of one token over its LPT lanes so
+// that the lane ends up with the full score of one head, returned. The head
+// a lane holds is own_head(s) for its position s in the token's lane group.
+template <int D, int HG>
+__device__ __forceinline__ float transpose_reduce(const float (&v)[HG], int s) {
+  using Geo = DecodeGeometry<D, HG>;
+  float a[HG];
+#pragma unroll
+  for (int g = 0; g < HG; ++g) a[g] = v[g];
+#pragma unroll
+  for (int k = 0; k < Geo::LOG_HG; ++k) {
+    const int off = Geo::LPT >> (k + 1);
+    const bool hi = (s & off) != 0;
+#pragma unroll
+    for (int i = 0; i < (HG >> (k + 1)); ++i) {
+      const float keep = hi ? a[i + (HG >> (k + 1))] : a[i];
+      const float send = hi ? a[i] : a[i + (HG >> (k + 1))];
+      a[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+#pragma unroll
+  for (int off = Geo::LPT >> (Geo::LOG_HG + 1); off > 0; off >>= 1)
+    a[0] += __shfl_xor_sync(kFull, a[0], off);
+  return a[0];
+}
+
+template <int D, int HG>
+__device__ __forceinline__ int own_head(int s) {
+  using Geo = DecodeGeometry<D, HG>;
+  int h = 0;
+#pragma unroll
+  for (int k = 0; k < Geo::LOG_HG; ++k)
+    if (s & (Geo::LPT >> (k + 1))) h += HG >> (k + 1);
+  return h;
+}
+
+// Position inside a token's lane group of the lane that holds head g.
+template <int D, int HG>
+__device__ __forceinline__ int owner_offset(int g) {
+  using Geo = DecodeGeometry<D, HG>;
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < Geo::LOG_HG; ++k)
+    if (g & (HG >> (k + 1))) s += Geo::LPT >> (k + 1);
+  return s;
+}
+
+// Per-warp running state of the online softmax.
+template <int D, int HG>
+struct WarpState {
+  static constexpr int NP = DecodeGeometry<D, HG>::DPL / 2;
+  float2 q[HG][NP];  // query slices, scaled by scale*log2(e)
+  float2 o[HG][NP];  // unnormalised output slices
+  float m;           // running max of this lane's own head (log2 units)
+  float l;           // running sum of this lane's own head
+};
+
+// One pass: every lane group handles one token of the chunk.
+template <int D, int HG, bool FULL>
+__device__ __forceinline__ void decode_pass(WarpState<D, HG>& st, const uint8_t* kbase,
+                                            const uint8_t* vbase, int tok, bool valid, int s,
+                                            int group_base) {
+  using Geo = DecodeGeometry<D, HG>;
+  constexpr int LPT = Geo::LPT, CPL = Geo::CPL;
+  const int row = tok < kChunk ? tok : kChunk - 1;
+  float2 acc[HG];
+#pragma unroll
+  for (int g = 0; g < HG; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(kbase + row * Geo::ROW + (c * LPT + s) * 16);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 k2 = bf16x2_to_float2(ws[e]);
+#pragma unroll
+      for (int g = 0; g < HG; ++g) acc[g] = __ffma2_rn(st.q[g][c * 4 + e], k2, acc[g]);
+    }
+  }
+  float part[HG];
+#pragma unroll
+  for (int g = 0; g < HG; ++g) part[g] = acc[g].x + acc[g].y;
+  float sc = transpose_reduce<D, HG>(part, s);
+  if (!FULL && !valid) sc = -INFINITY;
+
+  const float mn = fmaxf(st.m, sc);
+  const bool need = mn > st.m + kRescaleThreshold;
+  if (__any_sync(kFull, need)) {
+    const float alpha = need ? fast_exp2(st.m - mn) : 1.f;  // 0 when m = -inf
+    if (need) {
+      st.l *= alpha;
+      st.m = mn;
+    }
+#pragma unroll
+    for (int g = 0; g < HG; ++g) {
+      const float a = __shfl_sync(kFull, alpha, group_base + owner_offset<D, HG>(g));
+      const float2 a2 = make_float2(a, a);
+#pragma unroll
+      for (int i = 0; i < WarpState<D, HG>::NP; ++i) st.o[g][i] = __fmul2_rn(st.o[g][i], a2);
+    }
+  }
+  const float pr = (FULL || valid) ? fast_exp2(sc - st.m) : 0.f;
+  st.l += pr;
+  float pg[HG];
+#pragma unroll
+  for (int g = 0; g < HG; ++g) pg[g] = __shfl_sync(kFull, pr, group_base + owner_offset<D, HG>(g));
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    uint4 w = *reinterpret_cast<const uint4*>(vbase + row * Geo::ROW + (c * LPT + s) * 16);
+    if (!FULL && !valid) w = make_uint4(0u, 0u, 0u, 0u);  // masked rows may hold NaN
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 v2 = bf16x2_to_float2(ws[e]);
+#pragma unroll
+      for (int g = 0; g < HG; ++g)
+        st.o[g][c * 4 + e] = __ffma2_rn(v2, make_float2(pg[g], pg[g]), st.o[g][c * 4 + e]);
+    }
+  }
+}
+
+template <int D, int HG, int SPW, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
   using Geo = DecodeGeometry<D, HG>;
   constexpr int LPT = Geo::LPT, DPL = Geo::DPL, CPL = Geo::CPL, TPW = Geo::TPW;
+  constexpr int NP = DPL / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* slots = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * SPW * Geo::SLOT);
+  int* flag = reinterpret_cast<int*>(bars + kWarps * SPW);
+
+  // Everything below may read the pool the preceding KV write produces.
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -97,7 +238,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   const int nchunks = (kend - kbeg + kChunk - 1) / kChunk;
   const int my_chunks = (nchunks - warp + kWarps - 1) / kWarps;
 
-  const uint32_t full = 0xffffffffu;
   if (lane == 0) {
     for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[warp * SPW + s]), 1);
     fence_barrier_init();
@@ -134,15 +274,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   int32_t ids_next = load_ids(32);
   int issued = 0;
   for (int k = 0; k < SPW && k < my_chunks; ++k) {
-    const int32_t id = __shfl_sync(full, ids_cur, k);
+    const int32_t id = __shfl_sync(kFull, ids_cur, k);
     if (lane == 0) issue(k, id);
     ++issued;
   }
 
-  // query heads h0 .. h0+HG-1, this lane's slice of D, scaled by scale*log2(e)
   const int s = lane % LPT;
   const int tg = lane / LPT;
-  float q[HG][DPL];
+  const int group_base = tg * LPT;
+
+  WarpState<D, HG> st;
 #pragma unroll
   for (int g = 0; g < HG; ++g) {
     const uint4* qrow =
@@ -153,20 +294,15 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        q[g][c * 8 + 2 * e] = bf16_lo(ws[e]) * p.scale_log2;
-        q[g][c * 8 + 2 * e + 1] = bf16_hi(ws[e]) * p.scale_log2;
+        const float2 f = bf16x2_to_float2(ws[e]);
+        st.q[g][c * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
       }
     }
-  }
-  float o[HG][DPL];
-  float m[HG], l[HG];
 #pragma unroll
-  for (int g = 0; g < HG; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
+    for (int e = 0; e < NP; ++e) st.o[g][e] = make_float2(0.f, 0.f);
   }
+  st.m = -INFINITY;
+  st.l = 0.f;
 
   int kb = 0;
   int consumed = 0;
@@ -178,90 +314,32 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     }
     const int slot = k % SPW;
     const bool ok =
-        __all_sync(full, mbar_wait(smem_addr(&bars[warp * SPW + slot]), (k / SPW) & 1, p.status));
+        __all_sync(kFull, mbar_wait(smem_addr(&bars[warp * SPW + slot]), (k / SPW) & 1, p.status));
     if (!ok) break;
     consumed = k + 1;
-    const int32_t id = __shfl_sync(full, ids_cur, k - kb);
+    const int32_t id = __shfl_sync(kFull, ids_cur, k - kb);
     const bool chunk_ok = (id >= 0 && id < p.num_blocks);
     const int key0 = kbeg + (warp + k * kWarps) * kChunk;
     const uint8_t* kbase = slots + (warp * SPW + slot) * Geo::SLOT;
     const uint8_t* vbase = kbase + kChunk * Geo::ROW;
 
+    if (chunk_ok && key0 + kChunk <= kend && TPW <= kChunk) {
 #pragma unroll
-    for (int pass = 0; pass < Geo::NPASS; ++pass) {
-      const int tok = pass * TPW + tg;
-      const bool valid = chunk_ok && tok < kChunk && key0 + tok < kend;
-      const int row = tok < kChunk ? tok : kChunk - 1;
-      float sc[HG];
+      for (int pass = 0; pass < Geo::NPASS; ++pass)
+        decode_pass<D, HG, true>(st, kbase, vbase, pass * TPW + tg, true, s, group_base);
+    } else {
 #pragma unroll
-      for (int g = 0; g < HG; ++g) sc[g] = 0.f;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const uint4 w =
-            *reinterpret_cast<const uint4*>(kbase + row * Geo::ROW + (c * LPT + s) * 16);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float k0 = bf16_lo(ws[e]), k1 = bf16_hi(ws[e]);
-#pragma unroll
-          for (int g = 0; g < HG; ++g) {
-            sc[g] = fmaf(q[g][c * 8 + 2 * e], k0, sc[g]);
-            sc[g] = fmaf(q[g][c * 8 + 2 * e + 1], k1, sc[g]);
-          }
-        }
-      }
-#pragma unroll
-      for (int off = LPT / 2; off > 0; off >>= 1)
-#pragma unroll
-        for (int g = 0; g < HG; ++g) sc[g] += __shfl_xor_sync(full, sc[g], off);
-
-      bool need = false;
-      float mn[HG];
-#pragma unroll
-      for (int g = 0; g < HG; ++g) {
-        if (!valid) sc[g] = -INFINITY;
-        mn[g] = fmaxf(m[g], sc[g]);
-        need |= (mn[g] > m[g] + kRescaleThreshold);
-      }
-      if (__any_sync(full, need)) {
-#pragma unroll
-        for (int g = 0; g < HG; ++g) {
-          if (mn[g] > m[g] + kRescaleThreshold) {
-            const float alpha = fast_exp2(m[g] - mn[g]);  // 0 when m = -inf
-            l[g] *= alpha;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o[g][e] *= alpha;
-            m[g] = mn[g];
-          }
-        }
-      }
-      float pr[HG];
-#pragma unroll
-      for (int g = 0; g < HG; ++g) {
-        pr[g] = valid ? fast_exp2(sc[g] - m[g]) : 0.f;
-        l[g] += pr[g];
-      }
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        uint4 w = *reinterpret_cast<const uint4*>(vbase + row * Geo::ROW + (c * LPT + s) * 16);
-        if (!valid) w = make_uint4(0u, 0u, 0u, 0u);  // masked rows may hold NaN
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v0 = bf16_lo(ws[e]), v1 = bf16_hi(ws[e]);
-#pragma unroll
-          for (int g = 0; g < HG; ++g) {
-            o[g][c * 8 + 2 * e] = fmaf(pr[g], v0, o[g][c * 8 + 2 * e]);
-            o[g][c * 8 + 2 * e + 1] = fmaf(pr[g], v1, o[g][c * 8 + 2 * e + 1]);
-          }
-        }
+      for (int pass = 0; pass < Geo::NPASS; ++pass) {
+        const int tok = pass * TPW + tg;
+        const bool valid = chunk_ok && tok < kChunk && key0 + tok < kend;
+        decode_pass<D, HG, false>(st, kbase, vbase, tok, valid, s, group_base);
       }
     }
     __syncwarp();
     const int kn = k + SPW;
     if (kn < my_chunks) {
-      const int32_t idn = (kn - kb < 32) ? __shfl_sync(full, ids_cur, kn - kb)
-                                         : __shfl_sync(full, ids_next, kn - kb - 32);
+      const int32_t idn = (kn - kb < 32) ? __shfl_sync(kFull, ids_cur, kn - kb)
+                                         : __shfl_sync(kFull, ids_next, kn - kb - 32);
       if (lane == 0) {
         fence_proxy_async_smem();  // our reads of the slot precede the refill
         issue(kn, idn);
@@ -274,21 +352,29 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   for (int k = consumed; k < issued; ++k)
     mbar_wait(smem_addr(&bars[warp * SPW + (k % SPW)]), (k / SPW) & 1, nullptr);
 
+  // every lane gathers the running (m, l) of all HG heads of its token group
+  float m[HG], l[HG];
+#pragma unroll
+  for (int g = 0; g < HG; ++g) {
+    m[g] = __shfl_sync(kFull, st.m, group_base + owner_offset<D, HG>(g));
+    l[g] = __shfl_sync(kFull, st.l, group_base + owner_offset<D, HG>(g));
+  }
   // merge the warp's token groups (lanes tg differ) by xor shuffles
 #pragma unroll
   for (int off = LPT; off < 32; off <<= 1) {
 #pragma unroll
     for (int g = 0; g < HG; ++g) {
-      const float mo = __shfl_xor_sync(full, m[g], off);
-      const float lo = __shfl_xor_sync(full, l[g], off);
+      const float mo = __shfl_xor_sync(kFull, m[g], off);
+      const float lo = __shfl_xor_sync(kFull, l[g], off);
       const float M = fmaxf(m[g], mo);
       const float a = (m[g] == -INFINITY) ? 0.f : fast_exp2(m[g] - M);
       const float b = (mo == -INFINITY) ? 0.f : fast_exp2(mo - M);
       l[g] = a * l[g] + b * lo;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) {
-        const float oo = __shfl_xor_sync(full, o[g][e], off);
-        o[g][e] = a * o[g][e] + b * oo;
+      for (int e = 0; e < NP; ++e) {
+        const float ox = __shfl_xor_sync(kFull, st.o[g][e].x, off);
+        const float oy = __shfl_xor_sync(kFull, st.o[g][e].y, off);
+        st.o[g][e] = make_float2(a * st.o[g][e].x + b * ox, a * st.o[g][e].y + b * oy);
       }
       m[g] = M;
     }
@@ -303,8 +389,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
       for (int c = 0; c < CPL; ++c)
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          red_o[(warp * HG + g) * D + (c * LPT + s) * 8 + e] = o[g][c * 8 + e];
+        for (int e = 0; e < 4; ++e) {
+          float* dst = red_o + (warp * HG + g) * D + (c * LPT + s) * 8 + 2 * e;
+          dst[0] = st.o[g][c * 4 + e].x;
+          dst[1] = st.o[g][c * 4 + e].y;
+        }
       if (s == 0) {
         red_ml[(warp * HG + g) * 2] = m[g];
         red_ml[(warp * HG + g) * 2 + 1] = l[g];
@@ -341,41 +430,113 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       if (d == 0) p.ws_lse[r] = lse;
     }
   }
+  if (parts_i == 1) return;
+
+  // ---- split request: the last partition CTA of (request, head group) merges
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // publish this CTA's partial before counting it
+    const int old = atomicAdd(&p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x], 1);
+    *flag = (old == parts_i - 1);
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();  // see every other partition's partial
+  float* mg = red_ml;  // [HG] maxima of the partial lse (reuses shared memory)
+  const int64_t row0 = (int64_t)i * p.num_parts * p.num_heads;
+  for (int g = warp; g < HG; g += kWarps) {
+    float M = -INFINITY;
+    for (int pp = lane; pp < parts_i; pp += 32)
+      M = fmaxf(M, __ldcg(p.ws_lse + row0 + (int64_t)pp * p.num_heads + h0 + g));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0) mg[g] = M;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < HG * D / 4; idx += kWarps * 32) {
+    const int g = idx / (D / 4);
+    const int d4 = idx - g * (D / 4);
+    const float M = mg[g];
+    const int h = h0 + g;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int pp = 0; pp < parts_i; ++pp) {
+        const int64_t r = row0 + (int64_t)pp * p.num_heads + h;
+        const float w = fast_exp2((__ldcg(p.ws_lse + r) - M) * kLog2e);  // 0 for an empty part
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_out + r * D) + d4);
+        wsum += w;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    reinterpret_cast<float4*>(p.out + ((int64_t)t0 * p.num_heads + h) * D)[d4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (d4 == 0 && p.out_lse)
+      p.out_lse[(int64_t)t0 * p.num_heads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  }
+  if (threadIdx.x == 0) p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x] = 0;  // ready for reuse
 }
 
-template <int D, int HG, int SPW>
+template <int D, int HG, int SPW, int MINB>
 cudaError_t launch_decode_t(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream) {
   using Geo = DecodeGeometry<D, HG>;
-  const size_t smem = kWarps * SPW * Geo::SLOT + kWarps * SPW * sizeof(uint64_t);
+  const size_t smem = kWarps * SPW * Geo::SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, SPW>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, SPW, MINB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int group = p.num_heads / p.num_kv_heads;
-  const dim3 grid(p.num_kv_heads * (group / HG), p.num_parts, p.num_seqs);
-  decode_kernel<D, HG, SPW><<<grid, kWarps * 32, smem, stream>>>(kv_map, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_kv_heads * (group / HG), p.num_parts, p.num_seqs);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, HG, SPW, MINB>, kv_map, p);
 }
 
-constexpr int kSlotsPerWarp = 2;
+// Occupancy per shape: 3 CTAs per SM (168 registers per thread, 2 slots per
+// warp) where the working set fits, else 2 CTAs per SM with a deeper 3-slot
+// pipeline per warp (the 64 query + 64 output fp32 values per lane of the
+// larger head groups need ~210 registers).
+#ifndef PKV_DECODE_TIGHT_MINB
+#define PKV_DECODE_TIGHT_MINB 2
+#endif
+template <int D, int HG>
+struct DecodeOccupancy {
+  static constexpr bool kWide = (D == 128 && HG >= 2) || (D == 64 && HG >= 4);
+  static constexpr int MINB = kWide ? PKV_DECODE_TIGHT_MINB : 3;
+  static constexpr int SPW = MINB == 3 ? 2 : 3;
+};
+
+template <int D, int HG>
+cudaError_t launch_decode_g(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream) {
+  using Occ = DecodeOccupancy<D, HG>;
+  return launch_decode_t<D, HG, Occ::SPW, Occ::MINB>(p, kv_map, stream);
+}
 
 template <int D>
 cudaError_t launch_decode_d(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream) {
   const int group = p.num_heads / p.num_kv_heads;
-  if (group % 8 == 0) return launch_decode_t<D, 8, kSlotsPerWarp>(p, kv_map, stream);
-  if (group % 4 == 0) return launch_decode_t<D, 4, kSlotsPerWarp>(p, kv_map, stream);
-  if (group % 2 == 0) return launch_decode_t<D, 2, kSlotsPerWarp>(p, kv_map, stream);
-  return launch_decode_t<D, 1, kSlotsPerWarp>(p, kv_map, stream);
+  if (group % 8 == 0) return launch_decode_g<D, 8>(p, kv_map, stream);
+  if (group % 4 == 0) return launch_decode_g<D, 4>(p, kv_map, stream);
+  if (group % 2 == 0) return launch_decode_g<D, 2>(p, kv_map, stream);
+  return launch_decode_g<D, 1>(p, kv_map, stream);
 }
 
 }  // namespace
-
-size_t decode_smem_bytes(int head_dim) {
-  return (size_t)kWarps * kSlotsPerWarp * (2 * kChunk * head_dim * 2 + sizeof(uint64_t));
-}
 
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream) {
   if (p.head_dim == 128) return launch_decode_d<128>(p, kv_map, stream);

@@ -20,6 +20,8 @@ constexpr int kWarpsPerCta = 8;
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     kv_write_kernel(KvWriteParams p) {
+  griddep_wait();  // the previous step's attention may still read the pool
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (gw >= 2 * (int64_t)p.num_tokens) return;
@@ -53,8 +55,16 @@ cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream) {
   const int64_t warps = 2 * (int64_t)p.num_tokens;
   const int64_t ctas = (warps + kWarpsPerCta - 1) / kWarpsPerCta;
   if (ctas == 0) return cudaSuccess;
-  kv_write_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kWarpsPerCta * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_write_kernel, p);
 }
 
 }  // namespace pkv

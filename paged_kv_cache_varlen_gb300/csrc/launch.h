@@ -36,19 +36,17 @@ struct AttnParams {
   int32_t num_parts;          // partitions per request covering max_seq_len
   float* ws_out;              // [B][num_parts][H][D] (null when num_parts == 1)
   float* ws_lse;              // [B][num_parts][H]
+  int32_t* ws_cnt;            // [B][H] arrival counters, zero between calls
   int32_t* status;
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 
-// Decode kernel (query_len == 1 requests), CUDA cores, TMA-staged pages.
+// Decode kernel (query_len == 1 requests), CUDA cores, TMA-staged pages,
+// split-KV partitions merged in-kernel by the last partition CTA.
 // `kv_map` views the pool as [2*NB*BS rows][Hkv][D] with a box of
 // {D, 1, 16}.
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream);
-
-// Log-sum-exp merge of the decode kernel's partitions (requests whose
-// context spans more than one partition).
-cudaError_t launch_decode_merge(const AttnParams& p, cudaStream_t stream);
 
 // Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle;
@@ -61,8 +59,5 @@ cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,
                              const float* part_lse, int32_t num_parts, int64_t num_rows,
                              int32_t head_dim, cudaStream_t stream);
 
-// Shared-memory bytes a prefill CTA needs for this head_dim (for validation).
-size_t prefill_smem_bytes(int head_dim);
-size_t decode_smem_bytes(int head_dim);
 
 }  // namespace pkv

@@ -133,26 +133,6 @@ __global__ void __launch_bounds__(128)
   merge_row<1, NV>(v, D, out + row * D, out_lse ? out_lse + row : nullptr, nullptr);
 }
 
-// Decode split-KV merge: one CTA (4 warps) per (request, head) whose request
-// is a decode spanning more than one partition.
-template <int NV>
-__global__ void __launch_bounds__(128) decode_merge_kernel(AttnParams p) {
-  extern __shared__ float red[];
-  const int h = blockIdx.x;
-  const int i = blockIdx.y;
-  const int32_t t0 = p.cu_seqlens[i];
-  if (p.cu_seqlens[i + 1] - t0 != 1) return;  // not a decode request
-  const int32_t L = p.seq_lens[i];
-  if (L < 1 || L > p.max_seq_len) return;     // flagged by the decode kernel
-  const int parts = (L + p.part_size - 1) / p.part_size;
-  if (parts <= 1) return;                     // written directly by the decode kernel
-  const int D = p.head_dim;
-  const int64_t base = (int64_t)i * p.num_parts * p.num_heads + h;
-  RowView v{p.ws_out + base * D, p.ws_lse + base, (int64_t)p.num_heads * D, p.num_heads, parts};
-  merge_row<4, NV>(v, D, p.out + ((int64_t)t0 * p.num_heads + h) * D,
-                   p.out_lse ? p.out_lse + (int64_t)t0 * p.num_heads + h : nullptr, red);
-}
-
 }  // namespace
 
 cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,
@@ -169,13 +149,6 @@ cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,
   else
     lse_merge_kernel<4><<<grid, 128, 0, stream>>>(out, out_lse, part_out, part_lse, num_parts,
                                                   num_rows, head_dim);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_decode_merge(const AttnParams& p, cudaStream_t stream) {
-  const dim3 grid(p.num_heads, p.num_seqs);
-  const size_t smem = 4 * (p.head_dim + 1) * sizeof(float);
-  decode_merge_kernel<1><<<grid, 128, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

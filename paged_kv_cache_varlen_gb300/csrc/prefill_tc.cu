@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + Lay::BAR_OFF);
 
+  griddep_wait();  // the KV write (and all earlier work) has landed
+  griddep_launch_dependents();
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t full = 0xffffffffu;
@@ -449,15 +452,20 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
   const int G = p.num_heads / p.num_kv_heads;
   const int QT = kBM / G;
   const dim3 grid((p.max_query_len + QT - 1) / QT, p.num_kv_heads, p.num_seqs);
-  prefill_kernel<D><<<grid, kThreads, Lay::SMEM_ALLOC, stream>>>(q_map, kv_map, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Lay::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<D>, q_map, kv_map, p);
 }
 
 }  // namespace
-
-size_t prefill_smem_bytes(int head_dim) {
-  return head_dim == 128 ? PrefillLayout<128>::SMEM_ALLOC : PrefillLayout<64>::SMEM_ALLOC;
-}
 
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
                            const CUtensorMap& kv_map, cudaStream_t stream) {
