@@ -327,10 +327,7 @@ def run_ours(args):
     e2e_value = world * kv_bytes / (e2e_ms / E * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
-    nparts = 1 if args.partition_size == 0 else -(-w.max_seq_len // (args.partition_size
-                                                                       if args.partition_size > 0
-                                                                       else 512))
-    launches_per_step = 1 + 1 + (1 if nparts > 1 else 0) + (1 if w.max_query_len > 1 else 0)
+    launches_per_step = 2 + (1 if w.max_query_len > 1 else 0)  # write, decode, [prefill]
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         sample, desc = oracle_sample(w, args.cpu_seconds)

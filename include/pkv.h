@@ -123,8 +123,8 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  *                host never reads device tables; the grid is sized by them)
  *   scale        score scale, normally 1/sqrt(head_dim)
  *   partition_size  split-KV partition length in tokens for query_len == 1
- *                requests: 0 = never split; -1 = automatic (512 tokens,
- *                doubled until no request has more than 64 partitions);
+ *                requests: 0 = never split; -1 = automatic (1024 tokens,
+ *                doubled until no request has more than 32 partitions);
  *                > 0 = that many tokens, a multiple of 16. A split request's
  *                partitions are merged by log-sum-exp inside the same kernel
  *   workspace, workspace_bytes: scratch of at least

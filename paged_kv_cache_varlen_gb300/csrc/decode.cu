@@ -131,35 +131,49 @@ struct WarpState {
   float l;           // running sum of this lane's own head
 };
 
-// One pass: every lane group handles one token of the chunk.
+// One 16-token chunk. Each lane group owns NPASS tokens of the chunk (one per
+// pass). Phase A computes their scores (independent dot products and
+// transpose-reduces, so their latencies overlap), phase B makes one
+// online-softmax update for all of them, phase C accumulates P*V.
 template <int D, int HG, bool FULL>
-__device__ __forceinline__ void decode_pass(WarpState<D, HG>& st, const uint8_t* kbase,
-                                            const uint8_t* vbase, int tok, bool valid, int s,
-                                            int group_base) {
+__device__ __forceinline__ void decode_chunk(WarpState<D, HG>& st, const uint8_t* kbase,
+                                             const uint8_t* vbase, int key0, int kend,
+                                             bool chunk_ok, int s, int tg, int group_base) {
   using Geo = DecodeGeometry<D, HG>;
-  constexpr int LPT = Geo::LPT, CPL = Geo::CPL;
-  const int row = tok < kChunk ? tok : kChunk - 1;
-  float2 acc[HG];
+  constexpr int LPT = Geo::LPT, CPL = Geo::CPL, TPW = Geo::TPW, NPASS = Geo::NPASS;
+  float sc[NPASS];
+  bool valid[NPASS];
 #pragma unroll
-  for (int g = 0; g < HG; ++g) acc[g] = make_float2(0.f, 0.f);
+  for (int pass = 0; pass < NPASS; ++pass) {
+    const int tok = pass * TPW + tg;
+    valid[pass] = FULL || (chunk_ok && tok < kChunk && key0 + tok < kend);
+    const int row = tok < kChunk ? tok : kChunk - 1;
+    float2 acc[HG];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(kbase + row * Geo::ROW + (c * LPT + s) * 16);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int g = 0; g < HG; ++g) acc[g] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 k2 = bf16x2_to_float2(ws[e]);
+    for (int c = 0; c < CPL; ++c) {
+      const uint4 w =
+          *reinterpret_cast<const uint4*>(kbase + row * Geo::ROW + (c * LPT + s) * 16);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int g = 0; g < HG; ++g) acc[g] = __ffma2_rn(st.q[g][c * 4 + e], k2, acc[g]);
+      for (int e = 0; e < 4; ++e) {
+        const float2 k2 = bf16x2_to_float2(ws[e]);
+#pragma unroll
+        for (int g = 0; g < HG; ++g) acc[g] = __ffma2_rn(st.q[g][c * 4 + e], k2, acc[g]);
+      }
     }
-  }
-  float part[HG];
+    float part[HG];
 #pragma unroll
-  for (int g = 0; g < HG; ++g) part[g] = acc[g].x + acc[g].y;
-  float sc = transpose_reduce<D, HG>(part, s);
-  if (!FULL && !valid) sc = -INFINITY;
+    for (int g = 0; g < HG; ++g) part[g] = acc[g].x + acc[g].y;
+    sc[pass] = transpose_reduce<D, HG>(part, s);
+    if (!valid[pass]) sc[pass] = -INFINITY;
+  }
 
-  const float mn = fmaxf(st.m, sc);
+  float mx = sc[0];
+#pragma unroll
+  for (int pass = 1; pass < NPASS; ++pass) mx = fmaxf(mx, sc[pass]);
+  const float mn = fmaxf(st.m, mx);
   const bool need = mn > st.m + kRescaleThreshold;
   if (__any_sync(kFull, need)) {
     const float alpha = need ? fast_exp2(st.m - mn) : 1.f;  // 0 when m = -inf
@@ -175,22 +189,33 @@ __device__ __forceinline__ void decode_pass(WarpState<D, HG>& st, const uint8_t*
       for (int i = 0; i < WarpState<D, HG>::NP; ++i) st.o[g][i] = __fmul2_rn(st.o[g][i], a2);
     }
   }
-  const float pr = (FULL || valid) ? fast_exp2(sc - st.m) : 0.f;
-  st.l += pr;
-  float pg[HG];
+  float pr[NPASS];
 #pragma unroll
-  for (int g = 0; g < HG; ++g) pg[g] = __shfl_sync(kFull, pr, group_base + owner_offset<D, HG>(g));
+  for (int pass = 0; pass < NPASS; ++pass) {
+    pr[pass] = valid[pass] ? fast_exp2(sc[pass] - st.m) : 0.f;
+    st.l += pr[pass];
+  }
+
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    uint4 w = *reinterpret_cast<const uint4*>(vbase + row * Geo::ROW + (c * LPT + s) * 16);
-    if (!FULL && !valid) w = make_uint4(0u, 0u, 0u, 0u);  // masked rows may hold NaN
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  for (int pass = 0; pass < NPASS; ++pass) {
+    const int tok = pass * TPW + tg;
+    const int row = tok < kChunk ? tok : kChunk - 1;
+    float pg[HG];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 v2 = bf16x2_to_float2(ws[e]);
+    for (int g = 0; g < HG; ++g)
+      pg[g] = __shfl_sync(kFull, pr[pass], group_base + owner_offset<D, HG>(g));
 #pragma unroll
-      for (int g = 0; g < HG; ++g)
-        st.o[g][c * 4 + e] = __ffma2_rn(v2, make_float2(pg[g], pg[g]), st.o[g][c * 4 + e]);
+    for (int c = 0; c < CPL; ++c) {
+      uint4 w = *reinterpret_cast<const uint4*>(vbase + row * Geo::ROW + (c * LPT + s) * 16);
+      if (!valid[pass]) w = make_uint4(0u, 0u, 0u, 0u);  // masked rows may hold NaN
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v2 = bf16x2_to_float2(ws[e]);
+#pragma unroll
+        for (int g = 0; g < HG; ++g)
+          st.o[g][c * 4 + e] = __ffma2_rn(v2, make_float2(pg[g], pg[g]), st.o[g][c * 4 + e]);
+      }
     }
   }
 }
@@ -323,18 +348,10 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     const uint8_t* kbase = slots + (warp * SPW + slot) * Geo::SLOT;
     const uint8_t* vbase = kbase + kChunk * Geo::ROW;
 
-    if (chunk_ok && key0 + kChunk <= kend && TPW <= kChunk) {
-#pragma unroll
-      for (int pass = 0; pass < Geo::NPASS; ++pass)
-        decode_pass<D, HG, true>(st, kbase, vbase, pass * TPW + tg, true, s, group_base);
-    } else {
-#pragma unroll
-      for (int pass = 0; pass < Geo::NPASS; ++pass) {
-        const int tok = pass * TPW + tg;
-        const bool valid = chunk_ok && tok < kChunk && key0 + tok < kend;
-        decode_pass<D, HG, false>(st, kbase, vbase, tok, valid, s, group_base);
-      }
-    }
+    if (chunk_ok && key0 + kChunk <= kend && TPW <= kChunk)
+      decode_chunk<D, HG, true>(st, kbase, vbase, key0, kend, true, s, tg, group_base);
+    else
+      decode_chunk<D, HG, false>(st, kbase, vbase, key0, kend, chunk_ok, s, tg, group_base);
     __syncwarp();
     const int kn = k + SPW;
     if (kn < my_chunks) {

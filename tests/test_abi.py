@@ -48,17 +48,17 @@ def test_workspace_size_arithmetic(lib):
     # one partition: nothing to merge, no workspace
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 512, -1) == 0
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 0) == 0
-    # 4096 / 512 = 8 partitions: [B][8][H][D] fp32 partials + [B][8][H] fp32 lse
+    # 4096 / 1024 = 4 partitions: [B][4][H][D] fp32 partials + [B][4][H] fp32 lse
     # + [B][H] int32 merge counters, each piece 256-byte aligned
-    rows = 64 * 8 * 32
+    rows = 64 * 4 * 32
     up = lambda x: -(-x // 256) * 256
     expect = up(rows * 128 * 4) + up(rows * 4) + up(64 * 32 * 4)
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, -1) == expect
-    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 512) == expect
+    assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 1024) == expect
     # explicit partition must be a multiple of 16
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 100) == 0
-    # automatic partitions double until a request has at most 64 of them
-    rows = 8 * 64 * 32            # 131072 tokens -> 2048-token partitions -> 64 parts
+    # automatic partitions double until a request has at most 32 of them
+    rows = 8 * 32 * 32            # 131072 tokens -> 4096-token partitions -> 32 parts
     assert lib.pkv_attention_workspace_size(8, 8, 32, 8, 128, 131072, -1) == \
         up(rows * 128 * 4) + up(rows * 4) + up(8 * 32 * 4)
 
