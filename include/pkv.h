@@ -174,6 +174,38 @@ pkv_status pkv_lse_merge(float *out, float *out_lse, const float *part_out,
                          const float *part_lse, int32_t num_parts, int32_t num_tokens,
                          int32_t num_heads, int32_t head_dim, void *stream);
 
+/*
+ * pkv_paged_attention_varlen_noalloc -- pkv_paged_attention_varlen for
+ * callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is a packaging variant of the call
+ * above, not a step of the method.)
+ *
+ * Some callers cannot provide scratch memory: an engine whose memory manager
+ * already owns the whole GPU, a server that must not call cudaMalloc while
+ * it is serving, or a plugin that receives only its inputs and outputs. This
+ * call takes the same arguments as pkv_paged_attention_varlen without
+ * workspace / workspace_bytes and runs the same kernels; its split-KV
+ * scratch is a 16 MiB array built into the library, which every GPU that
+ * loads the library keeps until the process exits.
+ * - It allocates nothing (no cudaMalloc or cudaFree, no allocating library).
+ * - When the sizes would need more than 16 MiB of scratch (the value
+ *   pkv_attention_workspace_size returns), it returns PKV_ERR_WORKSPACE and
+ *   enqueues nothing; a larger partition_size lowers the need.
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture on
+ *   the device.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents: calls that may overlap on the GPU (other streams, other host
+ *   threads) race on it. The merge counters inside it are cleared by every
+ *   call.
+ */
+pkv_status pkv_paged_attention_varlen_noalloc(
+    float *out, float *out_lse, const void *q, const void *kv_pool, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+    int32_t num_seqs, int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float scale, int32_t partition_size, int32_t *dev_status, void *stream);
+
 /* Human-readable name of a pkv_status value (static storage). */
 const char *pkv_status_string(pkv_status status);
 

@@ -33,6 +33,9 @@ _SIGNATURES = {
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
     "pkv_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
+    "pkv_paged_attention_varlen_noalloc": (
+        _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
+        + [ctypes.c_float, _i32, _vp, _vp]),
     "pkv_status_string": (ctypes.c_char_p, [_i32]),
     "pkv_abi_version": (_i32, []),
 }
@@ -196,4 +199,47 @@ def lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, *,
     st = load_library().pkv_lse_merge(_ptr(out), _ptr(out_lse), _ptr(part_out), _ptr(part_lse),
                                       p, t, h, d, _stream(stream, part_out.device))
     _check(st, "lse_merge")
+    return out, out_lse
+
+
+def paged_attention_varlen_noalloc(q: torch.Tensor, kv_pool: torch.Tensor,
+                                   block_table: torch.Tensor, cu_seqlens: torch.Tensor,
+                                   seq_lens: torch.Tensor, max_query_len: int, max_seq_len: int,
+                                   *, out: torch.Tensor, out_lse: torch.Tensor | None = None,
+                                   scale: float | None = None, partition_size: int = -1,
+                                   dev_status: torch.Tensor | None = None, stream=None):
+    """:func:`paged_attention_varlen` for callers that cannot allocate.
+
+    For code that may not allocate device memory (its memory manager owns
+    the GPU, or it is not allowed to call cudaMalloc while serving): the
+    split-KV scratch comes from a fixed 16 MiB array inside the library, so
+    nothing is allocated here and ``out`` must be passed in. Raises
+    :class:`PkvError` (status 4) when the sizes need more scratch than that.
+    Calls that may overlap on the GPU share the array and race.
+    """
+    _need(q, torch.bfloat16, 3, "q")
+    _need(kv_pool, torch.bfloat16, 5, "kv_pool")
+    _need(block_table, torch.int32, 2, "block_table")
+    _need(cu_seqlens, torch.int32, 1, "cu_seqlens")
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    _need(out, torch.float32, 3, "out")
+    t, h, d = q.shape
+    _, nb, bs, hkv, d2 = kv_pool.shape
+    if d2 != d:
+        raise ValueError("q and kv_pool head_dim differ")
+    b = seq_lens.shape[0]
+    if cu_seqlens.shape[0] != b + 1 or block_table.shape[0] != b:
+        raise ValueError("cu_seqlens must be [B+1] and block_table [B, max_blocks]")
+    if out_lse is not None:
+        _need(out_lse, torch.float32, 2, "out_lse")
+    if dev_status is not None:
+        _need(dev_status, torch.int32, 1, "dev_status")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load_library().pkv_paged_attention_varlen_noalloc(
+        _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), _ptr(block_table),
+        block_table.shape[1], _ptr(cu_seqlens), _ptr(seq_lens), b, t, int(max_query_len),
+        int(max_seq_len), h, hkv, d, bs, nb, float(scale), int(partition_size),
+        _ptr(dev_status), _stream(stream, q.device))
+    _check(st, "paged_attention_varlen_noalloc")
     return out, out_lse
