@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target length of the oracle CPU-baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="target length of the whole --impl reference run")
     return ap.parse_args()
 
 
@@ -140,9 +142,56 @@ def dist_info():
     return world, rank, local
 
 
+SEEDS = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4, "mixed_step": 5}
+
+
+def rank_workload(config: str, rank: int, poison: bool = False):
+    """The batch one rank processes: the workload's own seed on rank 0, a
+    different seed per rank elsewhere (replicas see independent requests of
+    the same shape)."""
+    from paged_kv_cache_varlen_gb300 import workloads as wl
+
+    return wl.CONFIGS[config](seed=SEEDS[config] + 1000 * rank, poison=poison)
+
+
+def max_over_ranks(values: dict, dist=None, device="cpu") -> dict:
+    """Per-key maximum over ranks of this rank's timings: the slowest rank
+    sets the job's time. Without a process group the values come back as is."""
+    if dist is None:
+        return dict(values)
+    import torch
+
+    keys = sorted(values)
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(keys, t.tolist()))
+
+
+def job_throughput(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed in one step over the
+    slowest rank's step time (weak scaling: each rank keeps its own batch)."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
+def workload_config(w, partition_size: int, world: int) -> dict:
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "max_seq_len": w.max_seq_len,
+            "kv_bytes_per_step": w.kv_bytes(), "partition_size": partition_size,
+            "l2": "inputs larger than L2 (KV read per step >> 126 MB L2), no flush",
+            "parallelism": f"replicas x{world}"}
+
+
+def oracle_step(orc, w):
+    """One oracle step of the workload: the KV write, then attention of every
+    request (the whole hot path, in fp64 on the host cores)."""
+    pool = orc.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
+    orc.paged_attention(w.q, pool, w.block_table, w.cu_seqlens, w.seq_lens, w.scale)
+
+
 def oracle_step_seconds(w, budget_s: float):
-    """Time the oracle on whole steps of the workload (KV write + attention
-    of every request); repeat until about `budget_s` seconds of CPU time."""
+    """Time the oracle on whole steps of the workload; repeat until about
+    `budget_s` seconds of CPU time. Returns the median step time."""
     import oracle as oracle_pkg
 
     orc = oracle_pkg.load()
@@ -151,49 +200,69 @@ def oracle_step_seconds(w, budget_s: float):
     t_all = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        pool = orc.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
-        orc.paged_attention(w.q, pool, w.block_table, w.cu_seqlens, w.seq_lens, w.scale)
+        oracle_step(orc, w)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all >= budget_s or len(times) >= 50:
             break
     return statistics.median(times), cores, len(times)
 
 
-def oracle_sample(w, budget_s: float):
-    """A bounded sample of the workload for the oracle: the full batch when
-    one oracle step fits the budget, otherwise its first requests."""
+def work_units(w) -> np.ndarray:
+    """Keys scanned per request (context length x query rows), a proxy for
+    the oracle's time on it."""
+    return w.seq_lens.astype(np.int64) * w.query_lens.astype(np.int64)
+
+
+def oracle_sample(w, max_units: int = 4_000_000):
+    """A bounded sample of the workload for the oracle: the whole batch when
+    its work fits `max_units`, otherwise its first requests (at least one)."""
     from paged_kv_cache_varlen_gb300 import workloads as wl
 
-    work = int((w.seq_lens.astype(np.int64) * w.query_lens).sum())
-    if work <= 4_000_000:  # ~ a few seconds of fp64 work on a many-core host
-        return w, f"whole batch ({w.num_seqs} requests), repeated"
-    # keep requests in order until the key count reaches the cap
-    keep = np.searchsorted(np.cumsum(w.seq_lens.astype(np.int64) * w.query_lens), 4_000_000) + 1
-    keep = max(1, min(int(keep), w.num_seqs))
+    cum = np.cumsum(work_units(w))
+    if cum[-1] <= max_units:
+        return w, f"whole batch ({w.num_seqs} requests)"
+    keep = max(1, min(int(np.searchsorted(cum, max_units, side="right")), w.num_seqs))
     sub = wl.build(w.name + "_sample", w.seq_lens[:keep], w.query_lens[:keep], w.num_heads,
                    w.num_kv_heads, w.head_dim, w.block_size, seed=w.seed, poison=False)
-    return sub, f"first {keep} of {w.num_seqs} requests, repeated"
+    return sub, f"first {keep} of {w.num_seqs} requests"
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores.
+    W untimed and K timed steps, each over a bounded sample of the workload
+    sized so that the whole run takes about --ref-seconds. Under torchrun only
+    rank 0 runs it; the other ranks leave at once."""
     world, rank, _ = dist_info()
     if rank != 0:
         return 0
-    from paged_kv_cache_varlen_gb300 import workloads as wl
+    import oracle as oracle_pkg
 
-    w = wl.CONFIGS[args.config](poison=False)
-    sample, desc = oracle_sample(w, args.cpu_seconds)
-    steps_needed = max(1, args.steps)
-    sec, cores, n = oracle_step_seconds(sample, min(args.cpu_seconds, 60.0))
+    orc = oracle_pkg.load()
+    w = rank_workload(args.config, 0)
+    K, W = max(1, args.steps), max(3, args.warmup)
+    # size the sample from the time of the first request alone
+    first, _ = oracle_sample(w, 1)
+    t0 = time.perf_counter()
+    oracle_step(orc, first)
+    sec_per_unit = (time.perf_counter() - t0) / float(work_units(first).sum())
+    per_step = args.ref_seconds / (K + W)
+    sample, desc = oracle_sample(w, int(per_step / sec_per_unit))
+    for _ in range(W):
+        oracle_step(orc, sample)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_step(orc, sample)
+    sec = (time.perf_counter() - t0) / K
     gbs = sample.kv_bytes() / sec / 1e9
+    cores = orc.num_threads()
     line = {
         "impl": "reference", "metric": "paged decode attention KV GB/s", "value": gbs,
-        "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": 0, "ms_per_step": sec * 1e3,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "seqs_per_s": sample.num_seqs / sec,
-        "config": {"workload": w.name, "requested_steps": steps_needed},
+        "config": workload_config(w, args.partition_size, world),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "sample": f"{desc} of the rank-0 batch, every step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -220,10 +289,7 @@ def run_ours(args):
     pkv_build.build()
     pkv.load_library()
 
-    base = wl.CONFIGS[args.config]
-    seed_default = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4,
-                    "mixed_step": 5}[args.config]
-    w = base(seed=seed_default + 1000 * rank, poison=False)
+    w = rank_workload(args.config, rank)
     T, H, D = w.q.shape
 
     def bf16(a):
@@ -310,27 +376,20 @@ def run_ours(args):
     e2e_ms = e_start.elapsed_time(e_stop)
 
     # ---- reduce over ranks --------------------------------------------------
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    total_ms = max_over_ranks(total_ms)
-    e2e_ms = max_over_ranks(e2e_ms)
-    attn_avg_ms = max_over_ranks(attn_avg_ms)
+    slowest = max_over_ranks({"total_ms": total_ms, "e2e_ms": e2e_ms, "attn_avg_ms": attn_avg_ms},
+                             dist, dev)
+    total_ms, e2e_ms, attn_avg_ms = slowest["total_ms"], slowest["e2e_ms"], slowest["attn_avg_ms"]
 
     kv_bytes = w.kv_bytes()
     ms_per_step = total_ms / K
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
-    e2e_value = world * kv_bytes / (e2e_ms / E * 1e-3) / 1e9
+    value = job_throughput(world, kv_bytes, ms_per_step)
+    e2e_value = job_throughput(world, kv_bytes, e2e_ms / E)
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
     launches_per_step = 2 + (1 if w.max_query_len > 1 else 0)  # write, decode, [prefill]
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        sample, desc = oracle_sample(w, args.cpu_seconds)
+        sample, desc = oracle_sample(w)
         sec, cores, n = oracle_step_seconds(sample, args.cpu_seconds)
         cpu = {"value": sample.kv_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
                "kind": "oracle", "sample": f"{desc}; {n} oracle steps, median",
@@ -343,12 +402,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
             "pct_of_hbm_peak": 100.0 * value / world / peak,
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_heads": H,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": D,
-                       "block_size": w.block_size, "max_seq_len": w.max_seq_len,
-                       "kv_bytes_per_step": kv_bytes, "partition_size": args.partition_size,
-                       "l2": "inputs larger than L2 (KV read per step >> 126 MB L2), no flush",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(w, args.partition_size, world),
             "roofline": {"bound": "hbm", "kernel": "attention call (decode + split-KV merge)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak,

@@ -1,0 +1,97 @@
+"""bench.py's multi-rank host logic on CPU: two gloo ranks (no GPU).
+
+With torchrun every rank runs an independent replica; the job's time is the
+slowest rank's and its throughput counts the bytes of every rank. These tests
+run that reduction over a real two-process gloo group, check that the ranks
+get different batches of the same shape, and that the reference arm leaves
+rank 1 without doing any work.
+"""
+import json
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+WORLD = 2
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, port, out_dir):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench as b
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(WORLD), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD)
+    try:
+        mine = {"total_ms": 100.0 + 25.0 * rank, "e2e_ms": 300.0 - 40.0 * rank,
+                "attn_avg_ms": 0.5 + 0.25 * rank}
+        slowest = b.max_over_ranks(mine, dist, "cpu")
+        w = b.rank_workload("tiny", rank)
+        dist.barrier()
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"slowest": slowest, "world": b.dist_info()[0],
+                       "seq_lens": w.seq_lens.tolist(), "q_sum": int(w.q.astype(np.int64).sum()),
+                       "q_shape": list(w.q.shape), "kv_bytes": w.kv_bytes()}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.fixture(scope="module")
+def two_ranks(tmp_path_factory):
+    out_dir = str(tmp_path_factory.mktemp("ranks"))
+    mp.start_processes(_rank_main, args=(_free_port(), out_dir), nprocs=WORLD, join=True,
+                       start_method="spawn")
+    res = []
+    for r in range(WORLD):
+        with open(os.path.join(out_dir, f"rank{r}.json")) as f:
+            res.append(json.load(f))
+    return res
+
+
+def test_every_rank_sees_the_slowest_time(two_ranks):
+    want = {"total_ms": 125.0, "e2e_ms": 300.0, "attn_avg_ms": 0.75}
+    for r in two_ranks:
+        assert r["world"] == WORLD
+        assert r["slowest"] == want
+
+
+def test_replicas_get_independent_batches_of_one_shape(two_ranks):
+    a, b = two_ranks
+    assert a["q_shape"] == b["q_shape"] and a["seq_lens"] == b["seq_lens"]
+    assert a["kv_bytes"] == b["kv_bytes"]
+    assert a["q_sum"] != b["q_sum"]
+
+
+def test_job_throughput_counts_every_rank():
+    # 2 ranks x 1e9 bytes each in 0.5 ms per step -> 4000 GB/s for the job
+    assert bench.job_throughput(2, 10**9, 0.5) == pytest.approx(4000.0)
+    assert bench.job_throughput(1, 10**9, 0.5) == pytest.approx(2000.0)
+
+
+def test_no_group_means_local_values():
+    v = {"total_ms": 3.0}
+    assert bench.max_over_ranks(v) == v
+
+
+def test_reference_arm_rank1_does_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
+    assert bench.main() == 0
+    assert capsys.readouterr().out == ""
