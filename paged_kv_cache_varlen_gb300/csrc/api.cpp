@@ -187,6 +187,7 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.out = out;
   p.out_lse = out_lse;
   p.q = static_cast<const uint16_t*>(q);
+  p.kv_pool = kv_pool;
   p.block_table = block_table;
   p.cu_seqlens = cu_seqlens_q;
   p.seq_lens = seq_lens;

@@ -24,6 +24,7 @@ struct AttnParams {
   float* out;                 // [T][H][D] fp32
   float* out_lse;             // [T][H] fp32 or null
   const uint16_t* q;          // [T][H][D] bf16
+  const void* kv_pool;        // [2][NB][BS][Hkv][D] bf16
   const int32_t* block_table; // [B][max_blocks]
   const int32_t* cu_seqlens;  // [B+1]
   const int32_t* seq_lens;    // [B]
@@ -50,7 +51,8 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaSt
 
 // Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle;
-// `kv_map`: pool rows with a box of {64, 1, 16}, 128-byte swizzle.
+// `kv_map`: pool rows with a box of {64, 1, 16}, 128-byte swizzle (K pages);
+// V pages are read through p.kv_pool.
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
                            const CUtensorMap& kv_map, cudaStream_t stream);
 

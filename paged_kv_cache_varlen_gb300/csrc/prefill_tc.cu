@@ -20,11 +20,14 @@
 //     requests;
 //   * the Q tile is 128 rows = (128/G queries) x (G heads sharing the KV
 //     head), so one pass over the K/V pages serves the whole GQA group;
-//   * TMA tile loads with 128-byte swizzle: Q ({64, G, 128/G} boxes, double
-//     buffered across items), K and V tiles of 128 keys as eight 16-key paged
-//     boxes each whose physical block comes from block_table (no multicast),
-//     in separate 2-stage rings: a K stage is released as soon as its QK^T
-//     is done, a V stage after its PV;
+//   * Q arrives by TMA ({64, G, 128/G} boxes, 128-byte swizzle, double
+//     buffered across items). K and V tiles of 128 keys are gathered page by
+//     page (block ids from block_table) by two producer warps with 16-byte
+//     cp.async copies written straight into the 128-byte-swizzled layout the
+//     MMA descriptors read (keys past the needed range are zero-filled), in
+//     separate 2-stage rings: a K stage is released as soon as its QK^T is
+//     done, a V stage after its PV. (Paged 16-key TMA boxes were slower: the
+//     TMA unit takes ~200 cycles per 2 KB box per SM, cp.async ~12 B/cycle);
 //   * S = Q K^T (M=128, N=128, K=head_dim) and O += P V (M=128, N=head_dim,
 //     K=128) run as tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued
 //     by one thread; S is triple-buffered in tensor memory and P is written
@@ -37,8 +40,10 @@
 //     applies the causal mask and the exp2-domain online softmax (lazy
 //     rescale when the maximum grows by more than 8) and stores P; O is
 //     rescaled in TMEM when needed;
-//   * warp 4 produces TMA loads, warp 5 issues the MMAs; QK^T of tile j+1
-//     overlaps the softmax of tile j;
+//   * warps 4-5 produce loads, warp 6 issues the MMAs, polling so that QK^T
+//     of tile j+1 and PV of tile j each go as soon as their inputs are ready
+//     (QK^T first: the softmax waits for it); QK^T of tile j+1 overlaps the
+//     softmax of tile j;
 //   * every wait is bounded; on a timeout the CTA drains its copies and
 //     MMAs, frees its TMEM and leaves with PKV_DEV_TIMEOUT set.
 #include <math.h>
@@ -53,7 +58,9 @@ constexpr int kBM = 128;  // Q rows per tile
 constexpr int kBN = 128;  // keys per KV tile
 constexpr int kNS = 2;    // stages of each of the K and V rings
 constexpr int kSub = 16;  // keys per paged TMA box
-constexpr int kThreads = 192;
+constexpr int kProducers = 64;  // threads of the two K/V producer warps
+constexpr int kMmaWarp = 6;
+constexpr int kThreads = 224;   // 4 softmax warps, 2 producer warps, 1 MMA warp
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -196,16 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.num_heads / p.num_kv_heads;
   const int QT = kBM / G;  // queries per tile
 
-  // ---- setup: barriers (warp 4), work list (all), TMEM (warp 5)
+  // ---- setup: barriers (warp 4), work list (all), TMEM (MMA warp)
   if (warp == 4 && lane == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&bars->q_full[b]), 1);
       mbar_init(smem_addr(&bars->q_empty[b]), 1);
     }
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(smem_addr(&bars->k_full[s]), 1);
+      mbar_init(smem_addr(&bars->k_full[s]), kProducers);
       mbar_init(smem_addr(&bars->k_empty[s]), 1);
-      mbar_init(smem_addr(&bars->v_full[s]), 1);
+      mbar_init(smem_addr(&bars->v_full[s]), kProducers);
       mbar_init(smem_addr(&bars->v_empty[s]), 1);
     }
     for (int b = 0; b < 3; ++b) {
@@ -220,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int total = prefill_prefix(p, pref, bars->scan, QT) * p.num_kv_heads;  // syncs
   if ((int)blockIdx.x >= total) return;  // uniform; nothing allocated yet
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -234,105 +241,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t k_s = smem_addr(smem + Lay::K_OFF);
   const uint32_t v_s = smem_addr(smem + Lay::V_OFF);
 
-  if (warp == 4) {
-    // ================= TMA producer =================
-    const int32_t nrows = p.num_blocks * p.block_size;
-    if (lane == 0) {
-      prefetch_tmap(&q_map);
-      prefetch_tmap(&kv_map);
-    }
-    int gi = 0, gt = 0, k_issued = 0, v_issued = 0, q_issued = 0;
+  if (warp == 4 || warp == 5) {
+    // ============ producers: Q by TMA (one thread), K/V by cp.async (64 threads) ============
+    // Thread pt copies 16-byte piece pc of the rows of keys pk0, pk0 + KSTEP, ...
+    // of every tile into the 128-byte-swizzled layout the MMA descriptors
+    // expect (the piece at column unit u of row r lands at unit u ^ (r & 7)).
+    // Keys past the needed range and rows of bad blocks are filled with
+    // zeros (so V rows there never poison O).
+    constexpr int RP = D / 8;                // 16-byte pieces per K or V row
+    constexpr int KSTEP = kProducers / RP;   // keys per round
+    constexpr int NIT = kBN / KSTEP;         // rounds per tile
+    static_assert(kSub % KSTEP == 0, "a round stays inside one 16-key sub-block");
+    const int pt = threadIdx.x - 4 * 32;
+    const int pc = pt % RP;
+    const int pk0 = pt / RP;
+    const uint32_t col_off = (uint32_t)((pc >> 3) * Lay::CH_BYTES);
+    const uint32_t pcc = (uint32_t)(pc & 7);
+    const int64_t row_bytes = (int64_t)p.num_kv_heads * D * 2;
+    const uint8_t* pool = static_cast<const uint8_t*>(p.kv_pool);
+    const int64_t v_half = (int64_t)p.num_blocks * p.block_size * row_bytes;
+    const bool qlead = threadIdx.x == 4 * 32;
+    if (qlead) prefetch_tmap(&q_map);
+    int gi = 0, gt = 0, q_issued = 0, armed = 0;
     bool ok = true, bad_block = false;
     for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
       const PrefillItem d = prefill_item(p, pref, QT, it);
       const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
-      const int qb = gi & 1;
-      int w = 1;
-      if (lane == 0 && gi >= 2)
-        w = mbar_wait(smem_addr(&bars->q_empty[qb]), ((gi >> 1) - 1) & 1, p.status, abort);
-      ok = __shfl_sync(kFullMask, w, 0) != 0;
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_addr(&bars->q_full[qb]), Lay::TILE_BYTES);
-        for (int c = 0; c < Lay::NCH; ++c)
-          tma_load_3d(q_s + qb * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
-                      smem_addr(&bars->q_full[qb]), c * 64, d.kvh * G, d.t0 + d.j0);
+      if (warp == 4) {
+        const int qb = gi & 1;
+        int w = 1;
+        if (lane == 0 && gi >= 2)
+          w = mbar_wait(smem_addr(&bars->q_empty[qb]), ((gi >> 1) - 1) & 1, p.status, abort);
+        ok = __shfl_sync(kFullMask, w, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_addr(&bars->q_full[qb]), Lay::TILE_BYTES);
+          for (int c = 0; c < Lay::NCH; ++c)
+            tma_load_3d(q_s + qb * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
+                        smem_addr(&bars->q_full[qb]), c * 64, d.kvh * G, d.t0 + d.j0);
+        }
+        ++q_issued;
       }
-      ++q_issued;
+      const int64_t head_off = (int64_t)d.kvh * D * 2 + pc * 16;
       int32_t ids = -1;
       for (int j = 0; j < d.n_tiles; ++j, ++gt) {
-        if ((j & 3) == 0) {  // block ids of the next 4 tiles, one 16-key box per lane
+        if ((j & 3) == 0) {  // block ids of the next 4 tiles, one 16-key sub-block per lane
           const int key = (j * (kBN / kSub) + lane) * kSub;
           ids = (key < d.kv_end) ? __ldg(bt + key / p.block_size) : -1;
         }
-        int32_t sub_id[kBN / kSub];
-        uint32_t nvalid = 0;
+        // byte offset in the K half of the pool of each sub-block's first row
+        // for this thread's piece, or -1 (zero fill)
+        int64_t sub_off[kBN / kSub];
 #pragma unroll
         for (int sb = 0; sb < kBN / kSub; ++sb) {
-          sub_id[sb] = __shfl_sync(kFullMask, ids, (j & 3) * (kBN / kSub) + sb);
+          const int32_t id = __shfl_sync(kFullMask, ids, (j & 3) * (kBN / kSub) + sb);
           const int key = j * kBN + sb * kSub;
-          if (key >= d.kv_end) {
-            sub_id[sb] = -1;
-          } else if (sub_id[sb] < 0 || sub_id[sb] >= p.num_blocks) {
-            bad_block = true;
-            sub_id[sb] = -1;
-          } else {
-            ++nvalid;
+          sub_off[sb] = -1;
+          if (key < d.kv_end) {
+            if (id < 0 || id >= p.num_blocks)
+              bad_block = true;
+            else
+              sub_off[sb] = ((int64_t)id * p.block_size + key % p.block_size) * row_bytes + head_off;
           }
         }
         const int st = gt % kNS;
-        const uint32_t bytes = nvalid * kSub * 128 * Lay::NCH;
-        w = 1;
-        if (lane == 0 && gt >= kNS)
-          w = mbar_wait(smem_addr(&bars->k_empty[st]), ((gt / kNS) - 1) & 1, p.status, abort);
-        ok = __shfl_sync(kFullMask, w, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t kb = smem_addr(&bars->k_full[st]);
-          mbar_arrive_expect_tx(kb, bytes);
 #pragma unroll
-          for (int sb = 0; sb < kBN / kSub; ++sb) {
-            if (sub_id[sb] < 0) continue;
-            const int key = j * kBN + sb * kSub;
-            const int32_t row = sub_id[sb] * p.block_size + key % p.block_size;
-            for (int c = 0; c < Lay::NCH; ++c)
-              tma_load_3d(k_s + st * Lay::TILE_BYTES + c * Lay::CH_BYTES + sb * kSub * 128,
-                          &kv_map, kb, c * 64, d.kvh, row);
-          }
-        }
-        ++k_issued;
-        w = 1;
-        if (lane == 0 && gt >= kNS)
-          w = mbar_wait(smem_addr(&bars->v_empty[st]), ((gt / kNS) - 1) & 1, p.status, abort);
-        ok = __shfl_sync(kFullMask, w, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t vb = smem_addr(&bars->v_full[st]);
-          mbar_arrive_expect_tx(vb, bytes);
+        for (int half = 0; half < 2; ++half) {
+          uint64_t* empty = half ? &bars->v_empty[st] : &bars->k_empty[st];
+          uint64_t* full = half ? &bars->v_full[st] : &bars->k_full[st];
+          int w = 1;
+          if (lane == 0 && gt >= kNS)
+            w = mbar_wait(smem_addr(empty), ((gt / kNS) - 1) & 1, p.status, abort);
+          ok = __shfl_sync(kFullMask, w, 0) != 0;
+          if (!ok) break;
+          fence_proxy_async_smem();  // the MMAs' reads of this stage precede our writes
+          const uint32_t dst0 = (half ? v_s : k_s) + st * Lay::TILE_BYTES + col_off;
+          const int64_t base = half ? v_half : 0;
 #pragma unroll
-          for (int sb = 0; sb < kBN / kSub; ++sb) {
-            if (sub_id[sb] < 0) continue;
-            const int key = j * kBN + sb * kSub;
-            const int32_t row = sub_id[sb] * p.block_size + key % p.block_size + nrows;
-            for (int c = 0; c < Lay::NCH; ++c)
-              tma_load_3d(v_s + st * Lay::TILE_BYTES + c * Lay::CH_BYTES + sb * kSub * 128,
-                          &kv_map, vb, c * 64, d.kvh, row);
+          for (int i = 0; i < NIT; ++i) {
+            const int k = pk0 + KSTEP * i;
+            const int sb = (KSTEP * i) / kSub;
+            const bool valid = sub_off[sb] >= 0 && j * kBN + k < d.kv_end;
+            const uint8_t* src =
+                valid ? pool + base + sub_off[sb] + (int64_t)(k % kSub) * row_bytes : pool;
+            cp_async_16(dst0 + k * 128 + ((pcc ^ (uint32_t)(k & 7)) << 4), src, valid ? 16u : 0u);
           }
+          cp_async_arrive_noinc(smem_addr(full));
         }
-        ++v_issued;
+        if (!ok) break;
+        armed = gt + 1;
       }
     }
+    if (bad_block) set_status(p.status, PKV_DEV_BAD_BLOCK);
+    // our copies, and the barrier arrivals they trigger, land before the CTA can exit
+    cp_async_wait_all();
     if (lane == 0) {
-      if (bad_block) set_status(p.status, PKV_DEV_BAD_BLOCK);
-      // our copies in flight land before the CTA can exit
-      for (int g = max(0, k_issued - kNS); g < k_issued; ++g)
+      for (int g = max(0, armed - kNS); g < armed; ++g) {
         mbar_wait(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1, nullptr);
-      for (int g = max(0, v_issued - kNS); g < v_issued; ++g)
         mbar_wait(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1, nullptr);
-      for (int g = max(0, q_issued - 2); g < q_issued; ++g)
-        mbar_wait(smem_addr(&bars->q_full[g & 1]), (g >> 1) & 1, nullptr);
+      }
+      if (warp == 4)
+        for (int g = max(0, q_issued - 2); g < q_issued; ++g)
+          mbar_wait(smem_addr(&bars->q_full[g & 1]), (g >> 1) & 1, nullptr);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ================= MMA issuer (one thread) =================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false, false);
@@ -340,15 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int gi = 0, gt = 0;
       // S_g = Q K_g^T into S buffer g % 3 (P of tile g - 3 lived there)
-      auto issue_qk = [&](int g, uint32_t q_base) -> bool {
-        const int sb = g % 3;
-        if (g >= 3 &&
-            !mbar_wait(smem_addr(&bars->o_done[sb]), ((g / 3) - 1) & 1, p.status, abort))
-          return false;
-        if (!mbar_wait(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1, p.status, abort))
-          return false;
+      auto qk_ready = [&](int g) -> bool {
+        return (g < 3 || mbar_test(smem_addr(&bars->o_done[g % 3]), ((g / 3) - 1) & 1)) &&
+               mbar_test(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1);
+      };
+      auto issue_qk = [&](int g, uint32_t q_base) {
+        fence_proxy_async_smem();  // K was written by cp.async (generic proxy)
         tc_fence_after();
-        const uint32_t d_tmem = tmem + Lay::s_col(sb);
+        const uint32_t d_tmem = tmem + Lay::s_col(g % 3);
         const uint32_t kb = k_s + (g % kNS) * Lay::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -357,44 +368,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                   smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
         }
         umma_commit(smem_addr(&bars->k_empty[g % kNS]));
-        umma_commit(smem_addr(&bars->s_full[sb]));
-        return true;
+        umma_commit(smem_addr(&bars->s_full[g % 3]));
+      };
+      // O += P_g V_g (P as bf16 high parts, then the remainders)
+      auto issue_pv = [&](int g, bool first) {
+        fence_proxy_async_smem();  // V was written by cp.async (generic proxy)
+        tc_fence_after();
+        const uint32_t s_base = tmem + Lay::s_col(g % 3);
+        const uint32_t v_base = v_s + (g % kNS) * Lay::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
+          umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk), b, idesc_pv,
+                  (!first || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
+          umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
+        }
+        umma_commit(smem_addr(&bars->v_empty[g % kNS]));
+        umma_commit(smem_addr(&bars->o_done[g % 3]));
       };
       for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
         const PrefillItem d = prefill_item(p, pref, QT, it);
         const int qb = gi & 1;
         const uint32_t q_base = q_s + qb * Lay::TILE_BYTES;
         ok = mbar_wait(smem_addr(&bars->q_full[qb]), (gi >> 1) & 1, p.status, abort) &&
-             issue_qk(gt, q_base);
+             (gt < 3 || mbar_wait(smem_addr(&bars->o_done[gt % 3]), ((gt / 3) - 1) & 1, p.status,
+                                  abort)) &&
+             mbar_wait(smem_addr(&bars->k_full[gt % kNS]), (gt / kNS) & 1, p.status, abort);
+        if (!ok) break;
+        issue_qk(gt, q_base);
         for (int j = 0; ok && j < d.n_tiles; ++j) {
           const int g = gt + j;
-          if (j + 1 < d.n_tiles) {
-            ok = issue_qk(g + 1, q_base);
-            if (!ok) break;
-          } else {
-            umma_commit(smem_addr(&bars->q_empty[qb]));  // this item's Q is no longer read
+          // QK^T of the next tile and PV of this one, whichever can go first
+          // (QK^T first when both can: the softmax waits for it)
+          bool want_qk = j + 1 < d.n_tiles;
+          bool want_pv = true;
+          if (!want_qk) umma_commit(smem_addr(&bars->q_empty[qb]));  // Q no longer read
+          const uint64_t t0 = globaltimer();
+          for (uint32_t spin = 0; want_qk || want_pv; ++spin) {
+            if (want_qk && qk_ready(g + 1)) {
+              issue_qk(g + 1, q_base);
+              want_qk = false;
+              continue;
+            }
+            if (want_pv && mbar_test(smem_addr(&bars->p_ready), g & 1) &&
+                mbar_test(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1) &&
+                (j > 0 || gi == 0 || mbar_test(smem_addr(&bars->o_free), (gi - 1) & 1))) {
+              issue_pv(g, j == 0);  // the previous item's epilogue has read O
+              want_pv = false;
+              continue;
+            }
+            if ((spin & 63) == 63) {
+              if (*abort) {
+                ok = false;
+                break;
+              }
+              if (globaltimer() - t0 > PKV_WAIT_TIMEOUT_NS) {
+                set_status(p.status, PKV_DEV_TIMEOUT);
+                *abort = 1;
+                ok = false;
+                break;
+              }
+            }
           }
-          ok = mbar_wait(smem_addr(&bars->p_ready), g & 1, p.status, abort) &&
-               mbar_wait(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1, p.status, abort);
-          if (ok && j == 0 && gi > 0)  // the previous item's epilogue has read O
-            ok = mbar_wait(smem_addr(&bars->o_free), (gi - 1) & 1, p.status, abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t s_base = tmem + Lay::s_col(g % 3);
-          const uint32_t v_base = v_s + (g % kNS) * Lay::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-            umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk), b, idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-            umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
-          }
-          umma_commit(smem_addr(&bars->v_empty[g % kNS]));
-          umma_commit(smem_addr(&bars->o_done[g % 3]));
         }
         gt += d.n_tiles;
       }
@@ -468,22 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         l = l * alpha + rs;
-        if (j == d.n_tiles - 1 && (d.kv_end % kBN) != 0) {
-          // V rows past the last needed key may hold anything (NaN included);
-          // P is 0 there, and 0 * NaN would poison O, so zero them.
-          ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->v_full[gg % kNS]),
-                                               (gg / kNS) & 1, p.status, abort));
-          if (!ok) break;
-          if (j * kBN + r >= d.kv_end) {
-            uint8_t* vrow = smem + Lay::V_OFF + (gg % kNS) * Lay::TILE_BYTES + r * 128;
-#pragma unroll
-            for (int c = 0; c < Lay::NCH; ++c)
-#pragma unroll
-              for (int x = 0; x < 8; ++x)
-                reinterpret_cast<uint4*>(vrow + c * Lay::CH_BYTES)[x] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
         if (gg > 0) {
           // the previous tile's PV has finished writing O
           const int pv = gg - 1;
@@ -543,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: all tcgen05 work of the CTA is complete; release TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
