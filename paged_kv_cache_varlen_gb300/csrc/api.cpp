@@ -225,14 +225,11 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   if (pkv::launch_decode(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
 
   if (max_query_len > 1) {
-    CUtensorMap q_map, kv_sw;
+    CUtensorMap q_map;
     if (!encode_3d(&q_map, q, D, num_heads, num_tokens, D * 2, (uint64_t)num_heads * D * 2, 64,
                    (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
       return PKV_ERR_CUDA;
-    if (!encode_3d(&kv_sw, kv_pool, D, num_kv_heads, pool_rows, D * 2,
-                   (uint64_t)num_kv_heads * D * 2, 64, 1, 16, CU_TENSOR_MAP_SWIZZLE_128B))
-      return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(p, q_map, kv_sw, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

@@ -50,11 +50,9 @@ cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream);
 
 // Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
-// `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle;
-// `kv_map`: pool rows with a box of {64, 1, 16}, 128-byte swizzle (K pages);
-// V pages are read through p.kv_pool.
-cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
-                           const CUtensorMap& kv_map, cudaStream_t stream);
+// `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle.
+// K/V pages are gathered through p.kv_pool.
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream);
 
 // Public dense merge: part_out [P][T*H][D], part_lse [P][T*H].
 cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,

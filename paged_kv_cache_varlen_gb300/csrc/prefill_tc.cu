@@ -14,36 +14,43 @@
 // GB300 design:
 //   * persistent CTAs, one per SM: every CTA builds the per-request prefix
 //     sum of work items in shared memory and takes items blockIdx.x,
-//     blockIdx.x + gridDim.x, ...; an item is (request, KV head, tile of
-//     128/G queries), later query tiles (more keys) first. Tensor memory and
-//     barriers are set up once per CTA, and no CTA is launched for decode
-//     requests;
-//   * the Q tile is 128 rows = (128/G queries) x (G heads sharing the KV
-//     head), so one pass over the K/V pages serves the whole GQA group;
-//   * Q arrives by TMA ({64, G, 128/G} boxes, 128-byte swizzle, double
-//     buffered across items). K and V tiles of 128 keys are gathered page by
-//     page (block ids from block_table) by two producer warps with 16-byte
-//     cp.async copies written straight into the 128-byte-swizzled layout the
-//     MMA descriptors read (keys past the needed range are zero-filled), in
-//     separate 2-stage rings: a K stage is released as soon as its QK^T is
-//     done, a V stage after its PV. (Paged 16-key TMA boxes were slower: the
-//     TMA unit takes ~200 cycles per 2 KB box per SM, cp.async ~12 B/cycle);
+//     blockIdx.x + gridDim.x, ...; an item is (request, KV head, two
+//     consecutive query tiles A and B of 128/G queries each), later items
+//     (more keys) first. Tensor memory and barriers are set up once per CTA,
+//     and no CTA is launched for decode requests;
+//   * a Q tile is 128 rows = (128/G queries) x (G heads sharing the KV head),
+//     so one pass over the K/V pages serves the whole GQA group, and both Q
+//     tiles of the item share every K/V tile loaded: the gather from L2 (the
+//     bound of this kernel, ~12 B/cycle per SM) is paid once per two tiles;
+//   * Q arrives by TMA ({64, G, 128/G} boxes, 128-byte swizzle). K and V
+//     tiles of 128 keys are gathered page by page (block ids from
+//     block_table) by two producer warps with 16-byte cp.async copies
+//     written straight into the 128-byte-swizzled layout the MMA descriptors
+//     read (keys past the needed range are zero-filled), in separate 2-stage
+//     rings. (Paged 16-key TMA boxes were slower: ~200 cycles per 2 KB box
+//     per SM);
 //   * S = Q K^T (M=128, N=128, K=head_dim) and O += P V (M=128, N=head_dim,
 //     K=128) run as tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued
-//     by one thread; S is triple-buffered in tensor memory and P is written
-//     back in place over the S columns it came from, as a bf16 high part and
-//     a bf16 remainder (P ~= hi + lo to ~2^-16 relative; O accumulates
-//     hi*V + lo*V -- a single bf16 rounding of P puts few-key rows up to
-//     ~4e-3 off the exact result); P is the A operand straight from TMEM;
-//   * four softmax warps own one TMEM lane (= one Q row) per thread: pass 1
-//     reads S in 32-column pieces for the row maximum, pass 2 re-reads them,
-//     applies the causal mask and the exp2-domain online softmax (lazy
-//     rescale when the maximum grows by more than 8) and stores P; O is
-//     rescaled in TMEM when needed;
-//   * warps 4-5 produce loads, warp 6 issues the MMAs, polling so that QK^T
-//     of tile j+1 and PV of tile j each go as soon as their inputs are ready
-//     (QK^T first: the softmax waits for it); QK^T of tile j+1 overlaps the
-//     softmax of tile j;
+//     by one thread. Tensor memory holds S_A, S_B, O_A, O_B (4 x 128
+//     columns); P is written back in place over the S columns it came from,
+//     as a bf16 high part and a bf16 remainder (P ~= hi + lo to ~2^-16
+//     relative; O accumulates hi*V + lo*V -- a single bf16 rounding of P puts
+//     few-key rows up to ~4e-3 off the exact result); P is the A operand
+//     straight from TMEM;
+//   * two softmax warpgroups, one per Q tile; thread r of a warpgroup owns
+//     TMEM lane (= Q row) r: pass 1 reads S in 32-column pieces for the row
+//     maximum, pass 2 re-reads them, applies the causal mask and the
+//     exp2-domain online softmax (lazy rescale when the maximum grows by more
+//     than 8) and stores P; O is rescaled in TMEM when needed. While one
+//     warpgroup computes its softmax, the tensor core works on the other
+//     tile's products (ping-pong);
+//   * warps 8-9 produce loads, warp 10 issues the MMAs in a fixed order that
+//     alternates the two Q tiles (PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)),
+//     so one tile's softmax overlaps the other tile's products;
+//   * the softmax of a tile every key of which is visible to the warp's rows
+//     skips the mask and uses packed fp32x2 arithmetic; P's bf16 high part
+//     and remainder are cut by bit operations (truncation: hi + lo is p to
+//     2^-14 relative) instead of conversions;
 //   * every wait is bounded; on a timeout the CTA drains its copies and
 //     MMAs, frees its TMEM and leaves with PKV_DEV_TIMEOUT set.
 #include <math.h>
@@ -54,13 +61,16 @@
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;  // Q rows per tile
-constexpr int kBN = 128;  // keys per KV tile
-constexpr int kNS = 2;    // stages of each of the K and V rings
-constexpr int kSub = 16;  // keys per paged TMA box
-constexpr int kProducers = 64;  // threads of the two K/V producer warps
-constexpr int kMmaWarp = 6;
-constexpr int kThreads = 224;   // 4 softmax warps, 2 producer warps, 1 MMA warp
+constexpr int kBM = 128;                             // Q rows per tile
+constexpr int kQT = 2;                               // Q tiles per work item
+constexpr int kBN = 128;                             // keys per KV tile
+constexpr int kNS = 2;                               // stages of each of the K and V rings
+constexpr int kSub = 16;                             // keys per gathered sub-block
+constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 4*kQT-1
+constexpr int kProducers = 64;                       // two K/V producer warps
+constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // first producer warp (also issues Q)
+constexpr int kMmaWarp = kProdWarp0 + kProducers / 32;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -70,34 +80,35 @@ struct PrefillLayout {
   static constexpr int NCH = D / 64;                       // 128-byte column chunks of a row
   static constexpr int CH_BYTES = 128 * 128;               // one chunk of 128 rows
   static constexpr int TILE_BYTES = NCH * CH_BYTES;        // one Q, K or V tile
-  static constexpr int Q_OFF = 0;                          // [2] Q tiles
-  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;     // [kNS] K tiles
+  static constexpr int Q_OFF = 0;                          // [kQT] Q tiles of the item
+  static constexpr int K_OFF = Q_OFF + kQT * TILE_BYTES;   // [kNS] K tiles
   static constexpr int V_OFF = K_OFF + kNS * TILE_BYTES;   // [kNS] V tiles
   static constexpr int BAR_OFF = V_OFF + kNS * TILE_BYTES;
-  static constexpr int PREF_OFF = BAR_OFF + 256;
+  static constexpr int PREF_OFF = BAR_OFF + 512;
   // keep one CTA per SM (each CTA allocates all 512 TMEM columns)
   static size_t bytes(int num_seqs) {
     const size_t need = 1024 + PREF_OFF + (size_t)(num_seqs + 1) * 4;
     return need > 120 * 1024 ? need : 120 * 1024;
   }
-  // TMEM columns: S triple-buffered (P written in place), then O
-  __device__ static constexpr uint32_t s_col(int b) { return 128u * (uint32_t)b; }
-  static constexpr uint32_t O_COL = 384;
+  // TMEM columns: S of tile x (P written in place), then O of tile x
+  __device__ static constexpr uint32_t s_col(int x) { return 128u * (uint32_t)x; }
+  __device__ static constexpr uint32_t o_col(int x) { return 128u * (uint32_t)(kQT + x); }
   // P of keys 16*kk .. 16*kk+15 inside an S buffer: each 32-key piece holds
   // 16 columns of packed hi then 16 columns of packed lo
   __device__ static constexpr uint32_t p_hi_col(int kk) {
     return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
   }
 };
+static_assert(kQT * 2 * 128 <= (int)kTmemCols, "S and O of every Q tile fit in TMEM");
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full, q_empty;
   uint64_t k_full[kNS], k_empty[kNS];
   uint64_t v_full[kNS], v_empty[kNS];
-  uint64_t s_full[3];
-  uint64_t o_done[3];
-  uint64_t p_ready;
-  uint64_t o_free;
+  uint64_t s_full[kQT];   // QK^T of the tile landed in S_x
+  uint64_t p_ready[kQT];  // the warpgroup stored P_x (and rescaled O_x)
+  uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
+  uint64_t o_free[kQT];   // the warpgroup's epilogue has read O_x
   uint64_t mma_done;
   uint32_t tmem_base;
   int32_t abort;
@@ -108,9 +119,9 @@ struct PrefillItem {
   int req, kvh, j0, j1, t0, qlen, L, kv_end, n_tiles;
 };
 
-// Query tiles of request r (0 for decode requests); bad lengths flagged by
-// CTA 0.
-__device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QT, bool flag) {
+// Work units (pairs of query tiles) of request r (0 for decode requests);
+// bad lengths flagged by CTA 0. QP = queries per unit.
+__device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP, bool flag) {
   const int32_t t0 = __ldg(p.cu_seqlens + r), t1 = __ldg(p.cu_seqlens + r + 1);
   if (t0 < 0 || t1 < t0 || t1 > p.num_tokens) {
     if (flag) set_status(p.status, PKV_DEV_BAD_LENGTHS);
@@ -124,19 +135,19 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QT,
     if (flag) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return 0;
   }
-  return (qlen + QT - 1) / QT;
+  return (qlen + QP - 1) / QP;
 }
 
-// pref[r] = query tiles of requests before r; pref[B] = total. All threads.
+// pref[r] = work units of requests before r; pref[B] = total. All threads.
 __device__ __forceinline__ int prefill_prefix(const AttnParams& p, int* pref, int32_t* scan,
-                                              int QT) {
+                                              int QP) {
   const int B = p.num_seqs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool flag = blockIdx.x == 0;
   const int per = (B + kThreads - 1) / kThreads;
   const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
   int sum = 0;
-  for (int r = r0; r < r1; ++r) sum += prefill_units(p, r, QT, flag);
+  for (int r = r0; r < r1; ++r) sum += prefill_units(p, r, QP, flag);
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -150,14 +161,14 @@ __device__ __forceinline__ int prefill_prefix(const AttnParams& p, int* pref, in
   int run = base + incl - sum;
   for (int r = r0; r < r1; ++r) {
     pref[r] = run;
-    run += prefill_units(p, r, QT, false);
+    run += prefill_units(p, r, QP, false);
   }
   if (tid == kThreads - 1) pref[B] = run;
   __syncthreads();
   return pref[B];
 }
 
-__device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const int* pref, int QT,
+__device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const int* pref, int QP,
                                                     int it) {
   PrefillItem d;
   const int u = it / p.num_kv_heads;
@@ -174,10 +185,10 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
   d.t0 = __ldg(p.cu_seqlens + lo);
   d.qlen = __ldg(p.cu_seqlens + lo + 1) - d.t0;
   d.L = __ldg(p.seq_lens + lo);
-  const int ntq = (d.qlen + QT - 1) / QT;
-  const int qt = ntq - 1 - (u - pref[lo]);  // later (heavier) query tiles first
-  d.j0 = qt * QT;
-  d.j1 = min(d.qlen, d.j0 + QT);
+  const int ntq = (d.qlen + QP - 1) / QP;
+  const int qt = ntq - 1 - (u - pref[lo]);  // later (heavier) units first
+  d.j0 = qt * QP;
+  d.j1 = min(d.qlen, d.j0 + QP);
   d.kv_end = d.L - d.qlen + d.j1;  // keys [0, kv_end) are needed
   d.n_tiles = (d.kv_end + kBN - 1) / kBN;
   return d;
@@ -185,8 +196,7 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
-                   const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap q_map, const AttnParams p) {
   using Lay = PrefillLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
@@ -201,31 +211,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.num_heads / p.num_kv_heads;
-  const int QT = kBM / G;  // queries per tile
+  const int QT = kBM / G;   // queries per Q tile
+  const int QP = kQT * QT;  // queries per work item
 
-  // ---- setup: barriers (warp 4), work list (all), TMEM (MMA warp)
-  if (warp == 4 && lane == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_addr(&bars->q_full[b]), 1);
-      mbar_init(smem_addr(&bars->q_empty[b]), 1);
-    }
+  // ---- setup: barriers (first producer warp), work list (all), TMEM (MMA warp)
+  if (warp == kProdWarp0 && lane == 0) {
+    mbar_init(smem_addr(&bars->q_full), 1);
+    mbar_init(smem_addr(&bars->q_empty), 1);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(smem_addr(&bars->k_full[s]), kProducers);
       mbar_init(smem_addr(&bars->k_empty[s]), 1);
       mbar_init(smem_addr(&bars->v_full[s]), kProducers);
       mbar_init(smem_addr(&bars->v_empty[s]), 1);
     }
-    for (int b = 0; b < 3; ++b) {
-      mbar_init(smem_addr(&bars->s_full[b]), 1);
-      mbar_init(smem_addr(&bars->o_done[b]), 1);
+    for (int x = 0; x < kQT; ++x) {
+      mbar_init(smem_addr(&bars->s_full[x]), 1);
+      mbar_init(smem_addr(&bars->p_ready[x]), kBM);
+      mbar_init(smem_addr(&bars->o_done[x]), 1);
+      mbar_init(smem_addr(&bars->o_free[x]), kBM);
     }
-    mbar_init(smem_addr(&bars->p_ready), 128);
-    mbar_init(smem_addr(&bars->o_free), 128);
     mbar_init(smem_addr(&bars->mma_done), 1);
     bars->abort = 0;
     fence_barrier_init();
   }
-  const int total = prefill_prefix(p, pref, bars->scan, QT) * p.num_kv_heads;  // syncs
+  const int total = prefill_prefix(p, pref, bars->scan, QP) * p.num_kv_heads;  // syncs
   if ((int)blockIdx.x >= total) return;  // uniform; nothing allocated yet
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(&bars->tmem_base), kTmemCols);
@@ -241,18 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t k_s = smem_addr(smem + Lay::K_OFF);
   const uint32_t v_s = smem_addr(smem + Lay::V_OFF);
 
-  if (warp == 4 || warp == 5) {
-    // ============ producers: Q by TMA (one thread), K/V by cp.async (64 threads) ============
-    // Thread pt copies 16-byte piece pc of the rows of keys pk0, pk0 + KSTEP, ...
-    // of every tile into the 128-byte-swizzled layout the MMA descriptors
+  if (warp >= kProdWarp0 && warp < kMmaWarp) {
+    // ===== producers: Q by TMA (one thread), K/V by cp.async (64 threads) =====
+    // Thread pt copies 16-byte piece pc of the rows of keys pk0, pk0 + KSTEP,
+    // ... of every tile into the 128-byte-swizzled layout the MMA descriptors
     // expect (the piece at column unit u of row r lands at unit u ^ (r & 7)).
     // Keys past the needed range and rows of bad blocks are filled with
-    // zeros (so V rows there never poison O).
-    constexpr int RP = D / 8;                // 16-byte pieces per K or V row
-    constexpr int KSTEP = kProducers / RP;   // keys per round
-    constexpr int NIT = kBN / KSTEP;         // rounds per tile
+    // zeros (so V rows there never poison O: P is 0 there, 0 * NaN is not).
+    constexpr int RP = D / 8;               // 16-byte pieces per K or V row
+    constexpr int KSTEP = kProducers / RP;  // keys per round
+    constexpr int NIT = kBN / KSTEP;        // rounds per tile
     static_assert(kSub % KSTEP == 0, "a round stays inside one 16-key sub-block");
-    const int pt = threadIdx.x - 4 * 32;
+    const int pt = threadIdx.x - kSoftmaxThreads;
     const int pc = pt % RP;
     const int pk0 = pt / RP;
     const uint32_t col_off = (uint32_t)((pc >> 3) * Lay::CH_BYTES);
@@ -260,25 +269,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t row_bytes = (int64_t)p.num_kv_heads * D * 2;
     const uint8_t* pool = static_cast<const uint8_t*>(p.kv_pool);
     const int64_t v_half = (int64_t)p.num_blocks * p.block_size * row_bytes;
-    const bool qlead = threadIdx.x == 4 * 32;
+    const bool qlead = pt == 0;
     if (qlead) prefetch_tmap(&q_map);
-    int gi = 0, gt = 0, q_issued = 0, armed = 0;
+    int gi = 0, gt = 0, armed = 0, q_issued = 0;
     bool ok = true, bad_block = false;
     for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
-      const PrefillItem d = prefill_item(p, pref, QT, it);
+      const PrefillItem d = prefill_item(p, pref, QP, it);
       const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
-      if (warp == 4) {
-        const int qb = gi & 1;
+      if (warp == kProdWarp0) {
         int w = 1;
-        if (lane == 0 && gi >= 2)
-          w = mbar_wait(smem_addr(&bars->q_empty[qb]), ((gi >> 1) - 1) & 1, p.status, abort);
+        if (lane == 0 && gi >= 1)  // the previous item's QK^T products are done with Q
+          w = mbar_wait(smem_addr(&bars->q_empty), (gi - 1) & 1, p.status, abort);
         ok = __shfl_sync(kFullMask, w, 0) != 0;
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(smem_addr(&bars->q_full[qb]), Lay::TILE_BYTES);
-          for (int c = 0; c < Lay::NCH; ++c)
-            tma_load_3d(q_s + qb * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
-                        smem_addr(&bars->q_full[qb]), c * 64, d.kvh * G, d.t0 + d.j0);
+          // rows past the last token read as zeros; rows of the next request
+          // are loaded but belong to no valid output row
+          mbar_arrive_expect_tx(smem_addr(&bars->q_full), kQT * Lay::TILE_BYTES);
+          for (int x = 0; x < kQT; ++x)
+            for (int c = 0; c < Lay::NCH; ++c)
+              tma_load_3d(q_s + x * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
+                          smem_addr(&bars->q_full), c * 64, d.kvh * G, d.t0 + d.j0 + x * QT);
         }
         ++q_issued;
       }
@@ -340,9 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1, nullptr);
         mbar_wait(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1, nullptr);
       }
-      if (warp == 4)
-        for (int g = max(0, q_issued - 2); g < q_issued; ++g)
-          mbar_wait(smem_addr(&bars->q_full[g & 1]), (g >> 1) & 1, nullptr);
+      if (warp == kProdWarp0 && q_issued > 0)
+        mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer (one thread) =================
@@ -351,194 +361,239 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, D, false, true);
       bool ok = true;
       int gi = 0, gt = 0;
-      // S_g = Q K_g^T into S buffer g % 3 (P of tile g - 3 lived there)
-      auto qk_ready = [&](int g) -> bool {
-        return (g < 3 || mbar_test(smem_addr(&bars->o_done[g % 3]), ((g / 3) - 1) & 1)) &&
-               mbar_test(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1);
-      };
-      auto issue_qk = [&](int g, uint32_t q_base) {
+      // S_x = Q_x K_g^T (the K stage is released after the last Q tile's product)
+      auto issue_qk = [&](int x, int g) {
         fence_proxy_async_smem();  // K was written by cp.async (generic proxy)
         tc_fence_after();
-        const uint32_t d_tmem = tmem + Lay::s_col(g % 3);
+        const uint32_t d_tmem = tmem + Lay::s_col(x);
+        const uint32_t qb = q_s + x * Lay::TILE_BYTES;
         const uint32_t kb = k_s + (g % kNS) * Lay::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Lay::CH_BYTES + (kk & 3) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(q_base + off, 16, 1024),
+          umma_ss(d_tmem, smem_desc_sw128(qb + off, 16, 1024),
                   smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
         }
-        umma_commit(smem_addr(&bars->k_empty[g % kNS]));
-        umma_commit(smem_addr(&bars->s_full[g % 3]));
+        if (x == kQT - 1) umma_commit(smem_addr(&bars->k_empty[g % kNS]));
+        umma_commit(smem_addr(&bars->s_full[x]));
       };
-      // O += P_g V_g (P as bf16 high parts, then the remainders)
-      auto issue_pv = [&](int g, bool first) {
+      // O_x += P_x V_g (P as bf16 high parts, then the remainders)
+      auto issue_pv = [&](int x, int g, bool first) {
         fence_proxy_async_smem();  // V was written by cp.async (generic proxy)
         tc_fence_after();
-        const uint32_t s_base = tmem + Lay::s_col(g % 3);
+        const uint32_t s_base = tmem + Lay::s_col(x);
+        const uint32_t o_base = tmem + Lay::o_col(x);
         const uint32_t v_base = v_s + (g % kNS) * Lay::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk), b, idesc_pv,
-                  (!first || kk > 0) ? 1u : 0u);
+          umma_ts(o_base, s_base + Lay::p_hi_col(kk), b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(tmem + Lay::O_COL, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
+          umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
         }
-        umma_commit(smem_addr(&bars->v_empty[g % kNS]));
-        umma_commit(smem_addr(&bars->o_done[g % 3]));
+        if (x == kQT - 1) umma_commit(smem_addr(&bars->v_empty[g % kNS]));
+        umma_commit(smem_addr(&bars->o_done[x]));
+      };
+      // Fixed issue order per item: QK_A(0), QK_B(0), then for every tile j
+      // PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1). After the first tile this
+      // puts the two warpgroups half a period apart: the softmax of one Q
+      // tile runs while the tensor core works through the other tile's PV
+      // and next QK^T, instead of both softmaxes running at once and the
+      // tensor core idling meanwhile.
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_wait(smem_addr(bar), parity, p.status, abort);
       };
       for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
-        const PrefillItem d = prefill_item(p, pref, QT, it);
-        const int qb = gi & 1;
-        const uint32_t q_base = q_s + qb * Lay::TILE_BYTES;
-        ok = mbar_wait(smem_addr(&bars->q_full[qb]), (gi >> 1) & 1, p.status, abort) &&
-             (gt < 3 || mbar_wait(smem_addr(&bars->o_done[gt % 3]), ((gt / 3) - 1) & 1, p.status,
-                                  abort)) &&
-             mbar_wait(smem_addr(&bars->k_full[gt % kNS]), (gt / kNS) & 1, p.status, abort);
+        const PrefillItem d = prefill_item(p, pref, QP, it);
+        const int n = d.n_tiles;
+        ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
+        // S_x is free once PV of the previous item's last tile has completed
+        for (int x = 0; ok && x < kQT; ++x) {
+          if (gt > 0) ok = wait(&bars->o_done[x], (gt - 1) & 1);
+          if (!ok) break;
+          issue_qk(x, gt);
+        }
         if (!ok) break;
-        issue_qk(gt, q_base);
-        for (int j = 0; ok && j < d.n_tiles; ++j) {
+        if (n == 1) umma_commit(smem_addr(&bars->q_empty));  // Q of this item no longer read
+        for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j;
-          // QK^T of the next tile and PV of this one, whichever can go first
-          // (QK^T first when both can: the softmax waits for it)
-          bool want_qk = j + 1 < d.n_tiles;
-          bool want_pv = true;
-          if (!want_qk) umma_commit(smem_addr(&bars->q_empty[qb]));  // Q no longer read
-          const uint64_t t0 = globaltimer();
-          for (uint32_t spin = 0; want_qk || want_pv; ++spin) {
-            if (want_qk && qk_ready(g + 1)) {
-              issue_qk(g + 1, q_base);
-              want_qk = false;
-              continue;
-            }
-            if (want_pv && mbar_test(smem_addr(&bars->p_ready), g & 1) &&
-                mbar_test(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1) &&
-                (j > 0 || gi == 0 || mbar_test(smem_addr(&bars->o_free), (gi - 1) & 1))) {
-              issue_pv(g, j == 0);  // the previous item's epilogue has read O
-              want_pv = false;
-              continue;
-            }
-            if ((spin & 63) == 63) {
-              if (*abort) {
-                ok = false;
-                break;
-              }
-              if (globaltimer() - t0 > PKV_WAIT_TIMEOUT_NS) {
-                set_status(p.status, PKV_DEV_TIMEOUT);
-                *abort = 1;
-                ok = false;
-                break;
-              }
+          for (int x = 0; ok && x < kQT; ++x) {
+            // the first PV of an item overwrites O_x: the previous item's
+            // epilogue must have read it
+            ok = wait(&bars->p_ready[x], g & 1) &&
+                 wait(&bars->v_full[g % kNS], (g / kNS) & 1) &&
+                 (j > 0 || gi == 0 || wait(&bars->o_free[x], (gi - 1) & 1));
+            if (!ok) break;
+            issue_pv(x, g, j == 0);
+            if (j + 1 < n) {
+              // S_x holds P_x(j) until this PV completes
+              ok = wait(&bars->o_done[x], g & 1) &&
+                   wait(&bars->k_full[(g + 1) % kNS], ((g + 1) / kNS) & 1);
+              if (!ok) break;
+              issue_qk(x, g + 1);
+              if (x == kQT - 1 && j + 2 == n) umma_commit(smem_addr(&bars->q_empty));
             }
           }
         }
-        gt += d.n_tiles;
+        gt += n;
       }
       // every MMA issued so far has completed before TMEM is released
       umma_commit(smem_addr(&bars->mma_done));
       mbar_wait(smem_addr(&bars->mma_done), 0, nullptr);
     }
   } else {
-    // ================= softmax + epilogue: thread r owns Q row r =================
-    const int r = threadIdx.x;
-    const int rq = r / G;  // query of the row inside the tile
+    // ====== softmax + epilogue: warpgroup x owns Q tile x, thread r owns row r ======
+    const int x = warp >> 2;
+    const int r = threadIdx.x & (kBM - 1);
+    const int rq = r / G;  // query of the row inside its tile
     const int g = r % G;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t sa = tmem + lane_base + Lay::s_col(x);
+    const uint32_t oa = tmem + lane_base + Lay::o_col(x);
     const float sl2 = p.scale_log2;
     bool ok = true;
     int gt = 0;
     for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
-      const PrefillItem d = prefill_item(p, pref, QT, it);
-      const int qj = d.j0 + rq;
+      const PrefillItem d = prefill_item(p, pref, QP, it);
+      const int qj = d.j0 + x * QT + rq;
       const bool row_valid = qj < d.j1;
       const int pos = row_valid ? (d.L - d.qlen + qj) : (d.kv_end - 1);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < d.n_tiles; ++j) {
         const int gg = gt + j;
-        const int sb = gg % 3;
-        ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->s_full[sb]), (gg / 3) & 1,
-                                             p.status, abort));
+        ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->s_full[x]), gg & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sa = tmem + lane_base + Lay::s_col(sb);
         const int lim = pos - j * kBN;  // keys c <= lim of this tile are visible
-        // pass 1: row maximum over the visible keys
-        float mx = -INFINITY;
+        float alpha = 1.f, rs;
+        bool resc;
+        if (__all_sync(kFullMask, lim >= kBN - 1)) {
+          // ---- every key of the tile is visible to every row of the warp
+          // pass 1: row maximum (four independent chains)
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-        for (int ch = 0; ch < kBN / 32; ++ch) {
-          uint32_t u[32];
-          PKV_TMEM_LD32(sa + ch * 32, u);
-          tmem_wait_ld();
-          const int vis = lim - ch * 32;
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t u[32];
+            PKV_TMEM_LD32(sa + ch * 32, u);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c <= vis) mx = fmaxf(mx, __uint_as_float(u[c]));
-        }
-        const float mnew = fmaxf(m, mx * sl2);
-        float alpha = 1.f;
-        const bool resc = mnew > m + kRescaleThreshold;
-        if (resc) {
-          alpha = fast_exp2(m - mnew);  // 0 on the first tile
-          m = mnew;
-        }
-        // pass 2: probabilities, stored in place as packed bf16 hi | lo
-        float rs = 0.f;
-#pragma unroll 1
-        for (int ch = 0; ch < kBN / 32; ++ch) {
-          uint32_t u[32];
-          PKV_TMEM_LD32(sa + ch * 32, u);
-          tmem_wait_ld();
-          uint32_t pk[32];
-          const int vis = lim - ch * 32;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * c]), sl2, -m));
-            float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -m));
-            if (2 * c > vis) p0 = 0.f;
-            if (2 * c + 1 > vis) p1 = 0.f;
-            rs += p0 + p1;
-            pk[c] = pack_bf16x2(p0, p1);
-            pk[16 + c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
+            for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(u[c]));
           }
-          PKV_TMEM_ST32(sa + ch * 32, pk);
+          const float mnew = fmaxf(m, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
+          resc = mnew > m + kRescaleThreshold;
+          if (resc) {
+            alpha = fast_exp2(m - mnew);  // 0 on the first tile
+            m = mnew;
+          }
+          // pass 2: probabilities in place as packed bf16 hi | lo, where hi
+          // keeps the top 16 bits of p and lo = p - hi (exact) is truncated
+          // the same way: hi + lo is p to 2^-14 relative
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 negm = make_float2(-m, -m);
+          const float2 minus1 = make_float2(-1.f, -1.f);
+          float2 rsa = make_float2(0.f, 0.f), rsb = make_float2(0.f, 0.f);
+#pragma unroll 1
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t u[32];
+            PKV_TMEM_LD32(sa + ch * 32, u);
+            tmem_wait_ld();
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float2 x2 = __ffma2_rn(
+                  make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2, negm);
+              const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+              if (c & 1)
+                rsb = __fadd2_rn(rsb, p2);
+              else
+                rsa = __fadd2_rn(rsa, p2);
+              const uint32_t b0 = __float_as_uint(p2.x), b1 = __float_as_uint(p2.y);
+              const float2 hi2 = make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                             __uint_as_float(b1 & 0xffff0000u));
+              const float2 lo2 = __ffma2_rn(hi2, minus1, p2);
+              pk[c] = __byte_perm(b0, b1, 0x7632);
+              pk[16 + c] = __byte_perm(__float_as_uint(lo2.x), __float_as_uint(lo2.y), 0x7632);
+            }
+            PKV_TMEM_ST32(sa + ch * 32, pk);
+          }
+          tmem_wait_st();
+          rs = (rsa.x + rsb.x) + (rsa.y + rsb.y);
+        } else {
+          // ---- a diagonal tile: hide the keys after each row's position
+          // pass 1: row maximum over the visible keys
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t u[32];
+            PKV_TMEM_LD32(sa + ch * 32, u);
+            tmem_wait_ld();
+            const int vis = lim - ch * 32;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c <= vis) mx = fmaxf(mx, __uint_as_float(u[c]));
+          }
+          const float mnew = fmaxf(m, mx * sl2);
+          resc = mnew > m + kRescaleThreshold;
+          if (resc) {
+            alpha = fast_exp2(m - mnew);  // 0 on the first tile
+            m = mnew;
+          }
+          // pass 2: probabilities, stored in place as packed bf16 hi | lo
+          rs = 0.f;
+#pragma unroll 1
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t u[32];
+            PKV_TMEM_LD32(sa + ch * 32, u);
+            tmem_wait_ld();
+            uint32_t pk[32];
+            const int vis = lim - ch * 32;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * c]), sl2, -m));
+              float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -m));
+              if (2 * c > vis) p0 = 0.f;
+              if (2 * c + 1 > vis) p1 = 0.f;
+              rs += p0 + p1;
+              pk[c] = pack_bf16x2(p0, p1);
+              pk[16 + c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
+            }
+            PKV_TMEM_ST32(sa + ch * 32, pk);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
         l = l * alpha + rs;
         if (gg > 0) {
-          // the previous tile's PV has finished writing O
-          const int pv = gg - 1;
-          ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[pv % 3]), (pv / 3) & 1,
+          // the previous tile's PV has finished writing O_x
+          ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), (gg - 1) & 1,
                                                p.status, abort));
           if (!ok) break;
           tc_fence_after();
           if (j > 0 && __any_sync(kFullMask, resc)) {
-            const uint32_t oa = tmem + lane_base + Lay::O_COL;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t u[32];
               PKV_TMEM_LD32(oa + 32 * c, u);
               tmem_wait_ld();
 #pragma unroll
-              for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
               PKV_TMEM_ST32(oa + 32 * c, u);
             }
             tmem_wait_st();
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_addr(&bars->p_ready));
+        mbar_arrive(smem_addr(&bars->p_ready[x]));
       }
       if (!ok) break;
       // ---- epilogue of the item: O / l -> out, lse
       const int last = gt + d.n_tiles - 1;
-      ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[last % 3]), (last / 3) & 1,
-                                           p.status, abort));
+      ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), last & 1, p.status,
+                                           abort));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t oa = tmem + lane_base + Lay::O_COL;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float* orow = p.out + ((int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g) * D;
 #pragma unroll 1
@@ -548,17 +603,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 4)
-            *reinterpret_cast<float4*>(orow + 32 * c + x) =
-                make_float4(__uint_as_float(u[x]) * inv, __uint_as_float(u[x + 1]) * inv,
-                            __uint_as_float(u[x + 2]) * inv, __uint_as_float(u[x + 3]) * inv);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + 32 * c + e) =
+                make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
+                            __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
         }
       }
       if (row_valid && p.out_lse)
         p.out_lse[(int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g] =
             (m + fast_log2(l)) * kLn2;
       tc_fence_before();
-      mbar_arrive(smem_addr(&bars->o_free));  // the MMA may overwrite O now
+      mbar_arrive(smem_addr(&bars->o_free[x]));  // the MMA may overwrite O_x now
       gt += d.n_tiles;
     }
   }
@@ -574,8 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
-                             const CUtensorMap& kv_map, cudaStream_t stream) {
+cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream) {
   using Lay = PrefillLayout<D>;
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -592,8 +646,8 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int G = p.num_heads / p.num_kv_heads;
-  const int QT = kBM / G;
-  const int64_t bound = (int64_t)p.num_seqs * ((p.max_query_len + QT - 1) / QT) * p.num_kv_heads;
+  const int QP = kQT * (kBM / G);
+  const int64_t bound = (int64_t)p.num_seqs * ((p.max_query_len + QP - 1) / QP) * p.num_kv_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(bound < sms ? bound : sms));  // one CTA per SM (TMEM, smem)
   cfg.blockDim = dim3(kThreads);
@@ -604,15 +658,14 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, q_map, kv_map, p);
+  return cudaLaunchKernelEx(&cfg, kernel, q_map, p);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
-                           const CUtensorMap& kv_map, cudaStream_t stream) {
-  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, kv_map, stream);
-  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, kv_map, stream);
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream) {
+  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, stream);
+  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, stream);
   return cudaErrorInvalidValue;
 }
 
