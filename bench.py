@@ -65,6 +65,15 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("decode.cu", "merge.cu", "common.cuh"):
@@ -142,7 +151,8 @@ def dist_info():
     return world, rank, local
 
 
-SEEDS = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4, "mixed_step": 5}
+SEEDS = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4, "mixed_step": 5,
+         "prefill_chunks": 5}
 
 
 def rank_workload(config: str, rank: int, poison: bool = False):
@@ -387,6 +397,17 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
     launches_per_step = 2 + (1 if w.max_query_len > 1 else 0)  # write, decode, [prefill]
+    prefill_line = None
+    flops = w.attention_flops(2)
+    if flops > 0:
+        # chunked-prefill requests run on the tensor cores; the attention call
+        # also holds the decode kernel when the batch has decodes
+        tpeak, tkind = tensor_peak()
+        tflops = flops / (attn_avg_ms * 1e-3) / 1e12
+        prefill_line = {"flops_per_step": flops, "achieved_tflops": tflops, "peak_tflops": tpeak,
+                        "peak_kind": tkind, "frac": tflops / tpeak,
+                        "time": "attention call" + (" (decode kernel included)"
+                                                    if (w.query_lens == 1).any() else "")}
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         sample, desc = oracle_sample(w)
@@ -409,6 +430,7 @@ def run_ours(args):
                          "traffic": profiled_traffic(args.config)},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": e2e_ms / E},
+            "prefill": prefill_line,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
             "cpu_baseline": cpu,

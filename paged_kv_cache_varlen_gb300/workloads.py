@@ -290,12 +290,27 @@ def mixed_step(seed: int = 5, poison: bool = True, decodes: int = 48, chunks: in
                  meta={"token_budget": budget})
 
 
+def prefill_chunks(seed: int = 5, poison: bool = True, chunks: int = 4,
+                   chunk_len: int = 512) -> Workload:
+    """The prefill part of the mixed step on its own: the same 4 chunks of 512
+    queries over the same prior contexts (drawn exactly as mixed_step draws
+    them, after its 48 decode lengths); causal; 32/8, D 128."""
+    rng = np.random.default_rng(seed)
+    rng.integers(256, 8192, size=48, endpoint=True)  # mixed_step's decode lengths
+    prior = rng.integers(0, 8192, size=chunks, endpoint=True)
+    L = prior + chunk_len
+    ql = np.full(chunks, chunk_len)
+    return build("prefill_chunks", L, ql, 32, 8, 128, 16, seed=seed, rng=rng,
+                 max_blocks=-(-(8192 + chunk_len) // 16), poison=poison)
+
+
 CONFIGS = {
     "tiny": tiny,
     "llama3_8b_decode": llama_decode,
     "long_split_kv": long_decode,
     "prefix_cow": prefix_shared,
     "mixed_step": mixed_step,
+    "prefill_chunks": prefill_chunks,
 }
 
 
