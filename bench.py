@@ -152,7 +152,7 @@ def dist_info():
 
 
 SEEDS = {"tiny": 1, "llama3_8b_decode": 2, "long_split_kv": 3, "prefix_cow": 4, "mixed_step": 5,
-         "prefill_chunks": 5}
+         "prefill_chunks": 5, "spec_verify": 6}
 
 
 def rank_workload(config: str, rank: int, poison: bool = False):

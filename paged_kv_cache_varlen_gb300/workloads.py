@@ -304,6 +304,18 @@ def prefill_chunks(seed: int = 5, poison: bool = True, chunks: int = 4,
                  max_blocks=-(-(8192 + chunk_len) // 16), poison=poison)
 
 
+def spec_verify(seed: int = 6, poison: bool = True, batch: int = 64, lo_q: int = 2,
+                hi_q: int = 8) -> Workload:
+    """Speculative-decoding verification step on the Llama-3-8B decode shape:
+    batch 64, each request verifies q ~ U[2, 8] drafted tokens (causal among
+    them) over a context U[512, 4096] that includes them; 32/8, D 128."""
+    rng = np.random.default_rng(seed)
+    L = rng.integers(512, 4096, size=batch, endpoint=True)
+    ql = rng.integers(lo_q, hi_q, size=batch, endpoint=True)
+    return build("spec_verify", L, ql, 32, 8, 128, 16, seed=seed, rng=rng,
+                 max_blocks=4096 // 16, poison=poison)
+
+
 CONFIGS = {
     "tiny": tiny,
     "llama3_8b_decode": llama_decode,
@@ -311,6 +323,7 @@ CONFIGS = {
     "prefix_cow": prefix_shared,
     "mixed_step": mixed_step,
     "prefill_chunks": prefill_chunks,
+    "spec_verify": spec_verify,
 }
 
 

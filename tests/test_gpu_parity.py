@@ -15,7 +15,8 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["tiny", "llama3_8b_decode", "long_split_kv", "prefix_cow", "mixed_step", "prefill_chunks"]
+CONFIGS = ["tiny", "llama3_8b_decode", "long_split_kv", "prefix_cow", "mixed_step", "prefill_chunks",
+           "spec_verify"]
 
 
 @pytest.fixture(scope="module")
