@@ -52,6 +52,7 @@ typedef int32_t pkv_status;
 #define PKV_ERR_UNSUPPORTED 2       /* valid, but outside what the kernels implement */
 #define PKV_ERR_CUDA 3              /* a CUDA runtime call failed (e.g. launch) */
 #define PKV_ERR_WORKSPACE 4         /* workspace missing or smaller than required */
+#define PKV_ERR_NO_BLOCKS 5         /* the block pool cannot satisfy the request */
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define PKV_DEV_BAD_SLOT 1          /* slot_mapping entry outside [-1, num_blocks*block_size) */
@@ -205,6 +206,106 @@ pkv_status pkv_paged_attention_varlen_noalloc(
     int32_t num_seqs, int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
     int32_t num_blocks, float scale, int32_t partition_size, int32_t *dev_status, void *stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Host block manager and block copies -- the allocator side of the paged
+ * cache ([page 2] PagedAttention deep-dive: the physical block pool carved up
+ * at start-up; a block table per sequence mapping logical to physical blocks;
+ * a free block appended to a sequence's table when its last block is full;
+ * forking copies only the table, so the blocks are shared; a shared block
+ * gets its own copy when a sequence writes into it; the tables live on the
+ * CPU and are copied to the GPU for every step).
+ *
+ * Readings where the page is silent: the free pool is first-in first-out
+ * (the order given to pkv_bm_create, ascending ids by default; a block whose
+ * last reference goes away joins the back); a shared block is copied only
+ * when the writer's next token falls inside it (it is partially filled) -- a
+ * full shared block is never written again, so the next token goes to a
+ * fresh block without a copy; a copy covers the whole block, K and V.
+ *
+ * The manager is plain host memory and host code (no CUDA call); it is not
+ * thread-safe. Sequence ids are caller-chosen int64 values.
+ * ---------------------------------------------------------------------------
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of num_blocks blocks of block_size token slots. free_order
+ * (host, [num_blocks], nullable) is the initial order of the free pool and
+ * must be a permutation of 0..num_blocks-1. *out receives the handle.
+ * Errors: PKV_ERR_INVALID_ARG (bad sizes, not a permutation). */
+pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order,
+                         pkv_block_manager **out);
+void pkv_bm_destroy(pkv_block_manager *bm);
+
+/* A new, empty sequence. PKV_ERR_INVALID_ARG if the id exists. */
+pkv_status pkv_bm_add_seq(pkv_block_manager *bm, int64_t seq_id);
+
+/* child becomes a copy of parent's block table and length; every block it
+ * names gains a reference. PKV_ERR_INVALID_ARG for an unknown parent or an
+ * existing child. */
+pkv_status pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child);
+
+/* Drop the sequence; blocks left without references return to the pool. */
+pkv_status pkv_bm_free_seq(pkv_block_manager *bm, int64_t seq_id);
+
+/* Room for num_tokens more tokens of one sequence (host arrays):
+ *   slots      [num_tokens] int32, out: the slot of each new token, in order
+ *   copy_src, copy_dst [max_copies] int32, out: block copies to run (with
+ *              pkv_copy_blocks) before the tokens are written; an append makes
+ *              at most one; *num_copies receives the count
+ * All or nothing: PKV_ERR_NO_BLOCKS (the pool is short; nothing changes),
+ * PKV_ERR_INVALID_ARG (unknown sequence, missing output). */
+pkv_status pkv_bm_append(pkv_block_manager *bm, int64_t seq_id, int32_t num_tokens,
+                         int32_t *slots, int32_t *copy_src, int32_t *copy_dst, int32_t max_copies,
+                         int32_t *num_copies);
+
+/* One step for a batch (host arrays; the outputs are exactly the inputs of
+ * pkv_copy_blocks, pkv_kv_cache_write and pkv_paged_attention_varlen once
+ * copied to the device):
+ *   seq_ids     [num_seqs] int64, distinct existing sequences, in batch order
+ *   num_new     [num_seqs] int32, tokens each sequence adds this step (>= 0)
+ *   block_table [num_seqs][max_blocks] int32, out: tables, padded with -1
+ *   seq_lens    [num_seqs] int32, out: lengths including the new tokens
+ *   cu_seqlens  [num_seqs + 1] int32, out: prefix sums of num_new
+ *   slot_mapping [sum num_new] int32, out: slots of the new tokens
+ *   copy_src, copy_dst [max_copies] int32, out; *num_copies the count
+ * Appends happen in batch order (a copy taken by one sequence can leave a
+ * later sibling the sole owner of the shared block). All or nothing:
+ * PKV_ERR_NO_BLOCKS if the pool cannot hold the whole batch,
+ * PKV_ERR_INVALID_ARG for an unknown or repeated sequence, a table row too
+ * short for a sequence, or more copies than max_copies. */
+pkv_status pkv_bm_build_step(pkv_block_manager *bm, const int64_t *seq_ids, const int32_t *num_new,
+                             int32_t num_seqs, int32_t max_blocks, int32_t *block_table,
+                             int32_t *seq_lens, int32_t *cu_seqlens, int32_t *slot_mapping,
+                             int32_t *copy_src, int32_t *copy_dst, int32_t max_copies,
+                             int32_t *num_copies);
+
+/* Views: free blocks; a sequence's length (-1 if unknown); a block's
+ * reference count (-1 if out of range); a sequence's block table into
+ * table[capacity] (*num_blocks receives its length; PKV_ERR_WORKSPACE if
+ * capacity is too small). */
+int32_t pkv_bm_num_free(const pkv_block_manager *bm);
+int64_t pkv_bm_seq_len(const pkv_block_manager *bm, int64_t seq_id);
+int32_t pkv_bm_refcount(const pkv_block_manager *bm, int32_t block);
+pkv_status pkv_bm_block_table(const pkv_block_manager *bm, int64_t seq_id, int32_t *table,
+                              int32_t capacity, int32_t *num_blocks);
+
+/*
+ * pkv_copy_blocks -- copy whole blocks inside the pool (the device half of
+ * copy-on-write):
+ *   kv_pool            [2][num_blocks][block_size][num_kv_heads][head_dim] bf16
+ *   copy_src, copy_dst [num_copies] int32 (device)
+ * For each c: kv_pool[h][copy_dst[c]] = kv_pool[h][copy_src[c]] for h = K, V.
+ * Copies of one call must be independent (no block both a source and a
+ * destination); pkv_bm_build_step's copies are. num_copies == 0 is a no-op.
+ * Errors: PKV_DEV_BAD_BLOCK for an id outside [0, num_blocks) (that copy is
+ * skipped).
+ */
+pkv_status pkv_copy_blocks(void *kv_pool, const int32_t *copy_src, const int32_t *copy_dst,
+                           int32_t num_copies, int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t *dev_status,
+                           void *stream);
 
 /* Human-readable name of a pkv_status value (static storage). */
 const char *pkv_status_string(pkv_status status);

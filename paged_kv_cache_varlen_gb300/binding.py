@@ -36,6 +36,19 @@ _SIGNATURES = {
     "pkv_paged_attention_varlen_noalloc": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, _vp]),
+    "pkv_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pkv_bm_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
+    "pkv_bm_destroy": (None, [_vp]),
+    "pkv_bm_add_seq": (_i32, [_vp, ctypes.c_int64]),
+    "pkv_bm_fork": (_i32, [_vp, ctypes.c_int64, ctypes.c_int64]),
+    "pkv_bm_free_seq": (_i32, [_vp, ctypes.c_int64]),
+    "pkv_bm_append": (_i32, [_vp, ctypes.c_int64, _i32, _vp, _vp, _vp, _i32, _vp]),
+    "pkv_bm_build_step": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                 _vp]),
+    "pkv_bm_num_free": (_i32, [_vp]),
+    "pkv_bm_seq_len": (ctypes.c_int64, [_vp, ctypes.c_int64]),
+    "pkv_bm_refcount": (_i32, [_vp, _i32]),
+    "pkv_bm_block_table": (_i32, [_vp, ctypes.c_int64, _vp, _i32, _vp]),
     "pkv_status_string": (ctypes.c_char_p, [_i32]),
     "pkv_abi_version": (_i32, []),
 }
@@ -243,3 +256,115 @@ def paged_attention_varlen_noalloc(q: torch.Tensor, kv_pool: torch.Tensor,
         _ptr(dev_status), _stream(stream, q.device))
     _check(st, "paged_attention_varlen_noalloc")
     return out, out_lse
+
+
+def copy_blocks(kv_pool: torch.Tensor, copy_src: torch.Tensor, copy_dst: torch.Tensor, *,
+                dev_status: torch.Tensor | None = None, stream=None) -> None:
+    """Whole-block copies inside the pool (device int32 ``copy_src``/``copy_dst``),
+    the device half of copy-on-write; run before the step's KV write."""
+    _need(kv_pool, torch.bfloat16, 5, "kv_pool")
+    _need(copy_src, torch.int32, 1, "copy_src")
+    _need(copy_dst, torch.int32, 1, "copy_dst")
+    if copy_src.shape != copy_dst.shape:
+        raise ValueError("copy_src and copy_dst differ in length")
+    if dev_status is not None:
+        _need(dev_status, torch.int32, 1, "dev_status")
+    _, nb, bs, hkv, d = kv_pool.shape
+    st = load_library().pkv_copy_blocks(
+        _ptr(kv_pool), _ptr(copy_src), _ptr(copy_dst), copy_src.shape[0], nb, bs, hkv, d,
+        _ptr(dev_status), _stream(stream, kv_pool.device))
+    _check(st, "copy_blocks")
+
+
+class BlockManager:
+    """The host block manager of ``libpkv`` (native C++ behind the C ABI):
+    free pool, per-sequence block tables, fork and copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        import numpy as np
+
+        self._np = np
+        lib = load_library()
+        h = _vp()
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must hold every block id once")
+        st = lib.pkv_bm_create(num_blocks, block_size,
+                               order.ctypes.data if order is not None else None, ctypes.byref(h))
+        _check(st, "bm_create")
+        self._lib, self._h = lib, h
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq_id: int):
+        _check(self._lib.pkv_bm_add_seq(self._h, seq_id), "bm_add_seq")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pkv_bm_fork(self._h, parent, child), "bm_fork")
+
+    def free_seq(self, seq_id: int):
+        _check(self._lib.pkv_bm_free_seq(self._h, seq_id), "bm_free_seq")
+
+    def append(self, seq_id: int, num_tokens: int):
+        """Returns (slots, copies) like the reference manager."""
+        np = self._np
+        slots = np.zeros(max(num_tokens, 1), dtype=np.int32)
+        src = np.zeros(1, dtype=np.int32)
+        dst = np.zeros(1, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        st = self._lib.pkv_bm_append(self._h, seq_id, num_tokens, slots.ctypes.data,
+                                     src.ctypes.data, dst.ctypes.data, 1, ctypes.byref(n))
+        _check(st, "bm_append")
+        return slots[:num_tokens].tolist(), list(zip(src[:n.value].tolist(), dst[:n.value].tolist()))
+
+    def build_step(self, seq_ids, num_new, max_blocks: int):
+        """One batch: (block_table, seq_lens, cu_seqlens, slot_mapping, copy_src, copy_dst)
+        as numpy int32 arrays, ready to be copied to the device."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        nn = np.ascontiguousarray(num_new, dtype=np.int32)
+        b = ids.shape[0]
+        table = np.full((max(b, 1), max_blocks), -1, dtype=np.int32)
+        lens = np.zeros(max(b, 1), dtype=np.int32)
+        cu = np.zeros(b + 1, dtype=np.int32)
+        slots = np.zeros(max(int(nn.sum()), 1), dtype=np.int32)
+        cap = max(b, 1)
+        src = np.zeros(cap, dtype=np.int32)
+        dst = np.zeros(cap, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        st = self._lib.pkv_bm_build_step(
+            self._h, ids.ctypes.data, nn.ctypes.data, b, max_blocks, table.ctypes.data,
+            lens.ctypes.data, cu.ctypes.data, slots.ctypes.data, src.ctypes.data, dst.ctypes.data,
+            cap, ctypes.byref(n))
+        _check(st, "bm_build_step")
+        return (table[:b], lens[:b], cu, slots[:int(nn.sum())], src[:n.value], dst[:n.value])
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_bm_num_free(self._h))
+
+    def seq_len(self, seq_id: int) -> int:
+        return int(self._lib.pkv_bm_seq_len(self._h, seq_id))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_bm_refcount(self._h, block))
+
+    def block_table(self, seq_id: int):
+        np = self._np
+        n = ctypes.c_int32(0)
+        cap = max(self.num_blocks, 1)
+        out = np.zeros(cap, dtype=np.int32)
+        st = self._lib.pkv_bm_block_table(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n))
+        _check(st, "bm_block_table")
+        return out[:n.value].tolist()

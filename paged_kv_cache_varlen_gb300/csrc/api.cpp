@@ -106,6 +106,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_NO_BLOCKS: return "block pool exhausted";
     default: return "unknown status";
   }
 }
@@ -232,6 +233,24 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
     if (pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+pkv_status pkv_copy_blocks(void* kv_pool, const int32_t* copy_src, const int32_t* copy_dst,
+                           int32_t num_copies, int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t* dev_status,
+                           void* stream) {
+  if (num_copies < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_copies == 0) return PKV_OK;
+  if (!kv_pool || !copy_src || !copy_dst || !aligned16(kv_pool)) return PKV_ERR_INVALID_ARG;
+  const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_dim * 2;
+  if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_copies > 65535 || block_bytes / 16 / 1024 > 65535) return PKV_ERR_UNSUPPORTED;
+  return pkv::launch_copy_blocks(kv_pool, copy_src, copy_dst, num_copies, num_blocks,
+                                 block_bytes / 16, dev_status,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_lse_merge(float* out, float* out_lse, const float* part_out, const float* part_lse,

@@ -54,6 +54,12 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaSt
 // K/V pages are gathered through p.kv_pool.
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream);
 
+// Whole-block copies in the pool; block_vecs = 16-byte vectors in one
+// block of one half (K or V).
+cudaError_t launch_copy_blocks(void* pool, const int32_t* src, const int32_t* dst,
+                               int32_t num_copies, int32_t num_blocks, int64_t block_vecs,
+                               int32_t* status, cudaStream_t stream);
+
 // Public dense merge: part_out [P][T*H][D], part_lse [P][T*H].
 cudaError_t launch_lse_merge(float* out, float* out_lse, const float* part_out,
                              const float* part_lse, int32_t num_parts, int64_t num_rows,
