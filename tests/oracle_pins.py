@@ -358,6 +358,31 @@ def pin_merge_partitions_equal_full(oracle):
         np.testing.assert_allclose(lse, full_lse, rtol=0, atol=1e-12)
 
 
+def pin_cascade_prefix_plus_tail_equals_full(oracle):
+    """Decode requests sharing a copy-on-write prefix: attention over the
+    prefix alone (its blocks as their own table) merged by lse with attention
+    over each private tail (the table shifted past the prefix) equals the
+    attention over the whole context."""
+    P, BS = 32, 8
+    w = wl.build("cascade", [40, 33, 61, 45], [1, 1, 1, 1], 4, 2, 8, BS, seed=131,
+                 shared_prefix=[([0, 1, 2], P)])
+    pool = _written_pool(oracle, w)
+    full, full_lse = _attend(oracle, w, pool=pool)
+    members = [0, 1, 2]
+    cu1 = np.arange(len(members) + 1, dtype=np.int32)
+    ptable = np.repeat(w.block_table[:1, :P // BS], len(members), axis=0)
+    po, pl = oracle.paged_attention(w.q[members], pool, ptable, cu1,
+                                    np.full(len(members), P, np.int32), w.scale)
+    ttable = np.ascontiguousarray(w.block_table[members, P // BS:])
+    to, tl = oracle.paged_attention(w.q[members], pool, ttable, cu1,
+                                    (w.seq_lens[members] - P).astype(np.int32), w.scale)
+    out, lse = oracle.lse_merge(np.stack([po, to]), np.stack([pl, tl]))
+    np.testing.assert_allclose(out, full[members], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, full_lse[members], rtol=0, atol=1e-12)
+    # the prefix blocks really are shared by the group's tables
+    assert (w.block_table[members, :P // BS] == w.block_table[0, :P // BS]).all()
+
+
 def pin_merge_single_and_empty_partitions(oracle):
     rng = np.random.default_rng(121)
     o = rng.standard_normal((1, 5, 3, 8))
@@ -405,6 +430,7 @@ def pin_rejects_bad_inputs(oracle):
 
 
 ALL_PINS = [
+    pin_cascade_prefix_plus_tail_equals_full,
     pin_sizing_worked_example,
     pin_gqa_cache_fraction,
     pin_kv_write_closed_form,
