@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama3_8b_decode")
     ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--cascade", action="store_true",
+                    help="prefix_cow only: read each shared prefix once per group "
+                         "(pkv_cascade_decode) instead of once per request")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target length of the oracle CPU-baseline sample")
@@ -309,31 +312,50 @@ def run_ours(args):
         "q": bf16(w.q).pin_memory(), "k_new": bf16(w.k_new).pin_memory(),
         "v_new": bf16(w.v_new).pin_memory(),
         "slots": torch.from_numpy(w.slot_mapping).pin_memory(),
-        "table": torch.from_numpy(w.block_table).pin_memory(),
-        "cu": torch.from_numpy(w.cu_seqlens).pin_memory(),
-        "lens": torch.from_numpy(w.seq_lens).pin_memory(),
     }
+    ci = None
+    if args.cascade:
+        if "prefix_tokens" not in w.meta:
+            raise SystemExit("--cascade needs a workload with shared prefixes (prefix_cow)")
+        ci = wl.cascade_inputs(w, wl.prefix_groups(w))
+        for k in ("group_starts", "prefix_lens", "prefix_tables", "tail_tables", "tail_lens"):
+            host[k] = torch.from_numpy(ci[k]).pin_memory()
+    else:
+        host["table"] = torch.from_numpy(w.block_table).pin_memory()
+        host["cu"] = torch.from_numpy(w.cu_seqlens).pin_memory()
+        host["lens"] = torch.from_numpy(w.seq_lens).pin_memory()
     d = {k: v.to(dev) for k, v in host.items()}
     pool = bf16(w.pool).to(dev)
     out = torch.empty((T, H, D), dtype=torch.float32, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D, w.max_seq_len,
-                                            args.partition_size)
+    if ci is not None:
+        ws_bytes = pkv.cascade_workspace_size(w.num_seqs, len(ci["prefix_lens"]),
+                                              ci["max_group_size"], ci["max_prefix_len"],
+                                              ci["max_tail_len"], H, w.num_kv_heads, D)
+    else:
+        ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D,
+                                                w.max_seq_len, args.partition_size)
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(q, k_new, v_new, slots, table, cu, lens, ev=None):
-        pkv.kv_cache_write(pool, k_new, v_new, slots, stream=stream)
+    def step(dd, ev=None):
+        pkv.kv_cache_write(pool, dd["k_new"], dd["v_new"], dd["slots"], stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        pkv.paged_attention_varlen(q, pool, table, cu, lens, w.max_query_len, w.max_seq_len,
-                                   out=out, out_lse=lse, scale=w.scale,
-                                   partition_size=args.partition_size, workspace=ws,
-                                   stream=stream)
+        if ci is not None:
+            pkv.cascade_decode(dd["q"], pool, dd["group_starts"], dd["prefix_lens"],
+                               dd["prefix_tables"], ci["max_group_size"], ci["max_prefix_len"],
+                               dd["tail_tables"], dd["tail_lens"], ci["max_tail_len"], out=out,
+                               out_lse=lse, scale=w.scale, workspace=ws, stream=stream)
+        else:
+            pkv.paged_attention_varlen(dd["q"], pool, dd["table"], dd["cu"], dd["lens"],
+                                       w.max_query_len, w.max_seq_len, out=out, out_lse=lse,
+                                       scale=w.scale, partition_size=args.partition_size,
+                                       workspace=ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
-    dev_args = (d["q"], d["k_new"], d["v_new"], d["slots"], d["table"], d["cu"], d["lens"])
+    dev_args = (d,)
     for _ in range(max(3, args.warmup)):
         step(*dev_args)
     torch.cuda.synchronize(dev)
@@ -395,8 +417,12 @@ def run_ours(args):
     value = job_throughput(world, kv_bytes, ms_per_step)
     e2e_value = job_throughput(world, kv_bytes, e2e_ms / E)
     peak, peak_kind = hbm_peak()
-    achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
-    launches_per_step = 2 + (1 if w.max_query_len > 1 else 0)  # write, decode, [prefill]
+    # shared prefixes: the roofline counts every physical byte once (a prefix
+    # may legitimately be served from L2, or be read once per group)
+    roof_bytes = w.unique_kv_bytes() if "prefix_tokens" in w.meta else kv_bytes
+    achieved = roof_bytes / (attn_avg_ms * 1e-3) / 1e9
+    # write, decode, [prefill]; cascade: write, prepare, decode, prefix pass, merge
+    launches_per_step = 5 if ci is not None else 2 + (1 if w.max_query_len > 1 else 0)
     prefill_line = None
     flops = w.attention_flops(2)
     if flops > 0:
@@ -424,7 +450,11 @@ def run_ours(args):
             "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "config": workload_config(w, args.partition_size, world),
-            "roofline": {"bound": "hbm", "kernel": "attention call (decode + split-KV merge)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("cascade call (prefix pass + tail decode + merge)"
+                                    if ci is not None else
+                                    "attention call (decode + split-KV merge)"),
+                         "bytes_per_call": roof_bytes,
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak,
                          "traffic": profiled_traffic(args.config)},
@@ -435,6 +465,8 @@ def run_ours(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if ci is not None:
+            line["config"]["attention"] = "cascade: each shared prefix read once per group"
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

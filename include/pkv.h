@@ -208,6 +208,53 @@ pkv_status pkv_paged_attention_varlen_noalloc(
     int32_t num_blocks, float scale, int32_t partition_size, int32_t *dev_status, void *stream);
 
 /*
+ * pkv_cascade_decode -- decode attention for requests that share a
+ * copy-on-write prefix, reading each shared prefix once per group instead of
+ * once per request. ([page 2] PagedAttention deep-dive: forked sequences
+ * point at the same physical prompt blocks; [page 1] §07: attention over
+ * parts of the keys is combined exactly by log-sum-exp renormalisation.)
+ *
+ *   out      [num_seqs][num_heads][head_dim] fp32, out_lse [num_seqs][num_heads]
+ *            fp32 (nullable): exactly what pkv_paged_attention_varlen returns
+ *            for one decode query per request over its whole context
+ *   q        [num_seqs][num_heads][head_dim] bf16 (one query per request)
+ *   Prefix groups (device arrays): the requests of group g are
+ *            group_starts[g] .. group_starts[g+1]-1 ([num_prefix_groups + 1],
+ *            non-decreasing, within [0, num_seqs]; requests outside every
+ *            group have no prefix); prefix_lens [num_prefix_groups] tokens
+ *            (>= 0, a multiple of block_size); prefix_tables
+ *            [num_prefix_groups][max_prefix_blocks] the physical blocks of
+ *            each prefix. max_group_size >= the largest group, max_prefix_len
+ *            >= the largest prefix.
+ *   Tails (device arrays): tail_tables [num_seqs][max_tail_blocks] the blocks
+ *            of each request after its prefix, tail_lens [num_seqs] >= 1 (the
+ *            tail holds at least the new token), max_tail_len >= their max.
+ *   workspace: pkv_cascade_workspace_size(...) bytes, 256-byte aligned,
+ *            zero-filled before first use; left reusable (as for
+ *            pkv_paged_attention_varlen); one workspace per concurrent call.
+ * A request's context is its group's prefix followed by its tail. The prefix
+ * pass runs every group's queries (members x heads as the rows of tensor-core
+ * tiles) against the prefix blocks once, split into key segments; the tails
+ * run through the decode kernel; the partial results merge by log-sum-exp.
+ * Errors: as pkv_paged_attention_varlen; PKV_DEV_BAD_LENGTHS for inconsistent
+ * group_starts or lengths.
+ */
+size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_prefix_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len,
+                                  int32_t max_tail_len, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim);
+pkv_status pkv_cascade_decode(float *out, float *out_lse, const void *q, const void *kv_pool,
+                              int32_t num_prefix_groups, const int32_t *group_starts,
+                              const int32_t *prefix_lens, const int32_t *prefix_tables,
+                              int32_t max_prefix_blocks, int32_t max_group_size,
+                              int32_t max_prefix_len, const int32_t *tail_tables,
+                              int32_t max_tail_blocks, const int32_t *tail_lens,
+                              int32_t max_tail_len, int32_t num_seqs, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks, float scale, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * ---------------------------------------------------------------------------
  * Host block manager and block copies -- the allocator side of the paged
  * cache ([page 2] PagedAttention deep-dive: the physical block pool carved up

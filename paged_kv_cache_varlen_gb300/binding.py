@@ -36,6 +36,10 @@ _SIGNATURES = {
     "pkv_paged_attention_varlen_noalloc": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, _vp]),
+    "pkv_cascade_workspace_size": (ctypes.c_size_t, [_i32] * 8),
+    "pkv_cascade_decode": (
+        _i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _i32]
+        + [_i32] * 6 + [ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp]),
     "pkv_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "pkv_bm_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pkv_bm_destroy": (None, [_vp]),
@@ -368,3 +372,57 @@ class BlockManager:
         st = self._lib.pkv_bm_block_table(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n))
         _check(st, "bm_block_table")
         return out[:n.value].tolist()
+
+
+def cascade_workspace_size(num_seqs: int, num_prefix_groups: int, max_group_size: int,
+                           max_prefix_len: int, max_tail_len: int, num_heads: int,
+                           num_kv_heads: int, head_dim: int) -> int:
+    return int(load_library().pkv_cascade_workspace_size(
+        num_seqs, num_prefix_groups, max_group_size, max_prefix_len, max_tail_len, num_heads,
+        num_kv_heads, head_dim))
+
+
+def cascade_decode(q: torch.Tensor, kv_pool: torch.Tensor, group_starts: torch.Tensor,
+                   prefix_lens: torch.Tensor, prefix_tables: torch.Tensor, max_group_size: int,
+                   max_prefix_len: int, tail_tables: torch.Tensor, tail_lens: torch.Tensor,
+                   max_tail_len: int, *, out: torch.Tensor | None = None,
+                   out_lse: torch.Tensor | None = None, scale: float | None = None,
+                   workspace: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                   stream=None):
+    """Decode attention with copy-on-write prefixes read once per group
+    (see ``pkv_cascade_decode``). Allocates a zeroed workspace when none is given."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(kv_pool, torch.bfloat16, 5, "kv_pool")
+    for t, name in ((group_starts, "group_starts"), (prefix_lens, "prefix_lens"),
+                    (tail_lens, "tail_lens")):
+        _need(t, torch.int32, 1, name)
+    _need(prefix_tables, torch.int32, 2, "prefix_tables")
+    _need(tail_tables, torch.int32, 2, "tail_tables")
+    b, h, d = q.shape
+    _, nb, bs, hkv, d2 = kv_pool.shape
+    if d2 != d:
+        raise ValueError("q and kv_pool head_dim differ")
+    g = prefix_lens.shape[0]
+    if group_starts.shape[0] != g + 1 or prefix_tables.shape[0] != g:
+        raise ValueError("group_starts must be [G+1] and prefix_tables [G, max_prefix_blocks]")
+    if tail_tables.shape[0] != b or tail_lens.shape[0] != b:
+        raise ValueError("tail_tables and tail_lens must have one row per request")
+    if out is None:
+        out = torch.empty((b, h, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, 3, "out")
+    if out_lse is not None:
+        _need(out_lse, torch.float32, 2, "out_lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = cascade_workspace_size(b, g, int(max_group_size), int(max_prefix_len),
+                                  int(max_tail_len), h, hkv, d)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load_library().pkv_cascade_decode(
+        _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), g, _ptr(group_starts), _ptr(prefix_lens),
+        _ptr(prefix_tables), prefix_tables.shape[1], int(max_group_size), int(max_prefix_len),
+        _ptr(tail_tables), tail_tables.shape[1], _ptr(tail_lens), int(max_tail_len), b, h, hkv, d,
+        bs, nb, float(scale), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+        _stream(stream, q.device))
+    _check(st, "cascade_decode")
+    return out, out_lse

@@ -95,6 +95,47 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t he
   return w;
 }
 
+// Shared-prefix (cascade) decode: key segments per prefix so that the
+// prefix pass spreads over about a GPU's worth of CTAs (148 is a reference
+// count; the results do not depend on it).
+constexpr int64_t kCascadeRefSMs = 148;
+
+int32_t cascade_splits(int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len,
+                       int32_t num_heads, int32_t num_kv_heads) {
+  if (num_groups <= 0 || max_group_size <= 0 || max_prefix_len <= 0) return 1;
+  const int32_t qp = 2 * (128 / (num_heads / num_kv_heads));  // queries per prefill work item
+  const int64_t items = (int64_t)num_groups * ((max_group_size + qp - 1) / qp) * num_kv_heads;
+  const int64_t tiles = (max_prefix_len + 127) / 128;
+  int64_t s = (kCascadeRefSMs + items - 1) / items;
+  if (s > tiles) s = tiles;
+  return s < 1 ? 1 : (int32_t)s;
+}
+
+// Cascade workspace: partial outputs [S+1][B][H][D] fp32 and lse [S+1][B][H]
+// (S prefix segments, then the tail), the tail pass's cu_seqlens [B+1], then
+// the tail pass's own split-KV workspace (zero-filled once, like any
+// attention workspace).
+struct CascadeLayout {
+  int32_t splits;
+  size_t lse_off, cu_off, ws_off, ws_bytes, total;
+};
+
+CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_group_size,
+                             int32_t max_prefix_len, int32_t max_tail_len, int32_t num_heads,
+                             int32_t num_kv_heads, int32_t head_dim) {
+  CascadeLayout c{};
+  c.splits = cascade_splits(num_groups, max_group_size, max_prefix_len, num_heads, num_kv_heads);
+  const size_t rows = (size_t)(c.splits + 1) * num_seqs * num_heads;
+  c.lse_off = round_up(rows * head_dim * sizeof(float), 256);
+  c.cu_off = c.lse_off + round_up(rows * sizeof(float), 256);
+  c.ws_off = c.cu_off + round_up((size_t)(num_seqs + 1) * sizeof(int32_t), 256);
+  int32_t ps = 0, np = 1;
+  resolve_partition(max_tail_len, -1, &ps, &np);
+  c.ws_bytes = workspace_layout(num_seqs, num_heads, head_dim, np).total;
+  c.total = c.ws_off + c.ws_bytes;
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -208,6 +249,10 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.ws_out = nullptr;
   p.ws_lse = nullptr;
   p.ws_cnt = nullptr;
+  p.prefix_mode = 0;
+  p.kv_splits = 1;
+  p.split_out_stride = 0;
+  p.split_lse_stride = 0;
   if (need > 0) {
     p.ws_out = static_cast<float*>(workspace);
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_off);
@@ -249,6 +294,112 @@ pkv_status pkv_copy_blocks(void* kv_pool, const int32_t* copy_src, const int32_t
   return pkv::launch_copy_blocks(kv_pool, copy_src, copy_dst, num_copies, num_blocks,
                                  block_bytes / 16, dev_status,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_prefix_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len,
+                                  int32_t max_tail_len, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  if (num_heads % num_kv_heads != 0) return 0;
+  return cascade_layout(num_seqs, num_prefix_groups, max_group_size, max_prefix_len, max_tail_len,
+                        num_heads, num_kv_heads, head_dim)
+      .total;
+}
+
+pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const void* kv_pool,
+                              int32_t num_prefix_groups, const int32_t* group_starts,
+                              const int32_t* prefix_lens, const int32_t* prefix_tables,
+                              int32_t max_prefix_blocks, int32_t max_group_size,
+                              int32_t max_prefix_len, const int32_t* tail_tables,
+                              int32_t max_tail_blocks, const int32_t* tail_lens,
+                              int32_t max_tail_len, int32_t num_seqs, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks, float scale, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_prefix_groups < 0) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !kv_pool || !tail_tables || !tail_lens) return PKV_ERR_INVALID_ARG;
+  if (num_prefix_groups > 0 && (!group_starts || !prefix_lens || !prefix_tables ||
+                                max_prefix_blocks <= 0 || max_group_size <= 0 ||
+                                max_prefix_len < 0))
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (max_tail_len < 1 || max_tail_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  const int32_t group = num_heads / num_kv_heads;
+  if (num_prefix_groups > 0 && max_prefix_len > 0 && (group > 128 || (128 % group) != 0))
+    return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_prefix_blocks * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const CascadeLayout c = cascade_layout(num_seqs, num_prefix_groups, max_group_size,
+                                         max_prefix_len, max_tail_len, num_heads, num_kv_heads,
+                                         head_dim);
+  if (!workspace || workspace_bytes < c.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PKV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* part_out = reinterpret_cast<float*>(ws);
+  float* part_lse = reinterpret_cast<float*>(ws + c.lse_off);
+  int32_t* tail_cu = reinterpret_cast<int32_t*>(ws + c.cu_off);
+  const int64_t bh = (int64_t)num_seqs * num_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // 1. empty prefix partials, one query per request for the tail pass
+  if (pkv::launch_cascade_prepare(part_lse, (int64_t)c.splits * bh, tail_cu, num_seqs, st) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  // 2. tails: ordinary decode over each request's private blocks
+  pkv_status s = pkv_paged_attention_varlen(
+      part_out + (int64_t)c.splits * bh * head_dim, part_lse + (int64_t)c.splits * bh, q, kv_pool,
+      tail_tables, max_tail_blocks, tail_cu, tail_lens, num_seqs, num_seqs, 1, max_tail_len,
+      num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, -1,
+      c.ws_bytes > 0 ? ws + c.ws_off : nullptr, c.ws_bytes, dev_status, stream);
+  if (s != PKV_OK) return s;
+  // 3. prefixes: every group's queries against its shared blocks, once, on
+  //    the tensor cores (the prefill kernel in prefix mode), cut into key
+  //    segments
+  if (num_prefix_groups > 0 && max_prefix_len > 0) {
+    AttnParams p;
+    p.out = part_out;
+    p.out_lse = part_lse;
+    p.q = static_cast<const uint16_t*>(q);
+    p.kv_pool = kv_pool;
+    p.block_table = prefix_tables;
+    p.cu_seqlens = group_starts;
+    p.seq_lens = prefix_lens;
+    p.max_blocks = max_prefix_blocks;
+    p.num_seqs = num_prefix_groups;
+    p.num_tokens = num_seqs;
+    p.max_query_len = max_group_size;
+    p.max_seq_len = max_prefix_len;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.part_size = 0;
+    p.num_parts = 1;
+    p.ws_out = nullptr;
+    p.ws_lse = nullptr;
+    p.ws_cnt = nullptr;
+    p.status = dev_status;
+    p.prefix_mode = 1;
+    p.kv_splits = c.splits;
+    p.split_out_stride = bh * head_dim;
+    p.split_lse_stride = bh;
+    const uint64_t D = (uint64_t)head_dim;
+    CUtensorMap q_map;
+    if (!encode_3d(&q_map, q, D, num_heads, num_seqs, D * 2, (uint64_t)num_heads * D * 2, 64,
+                   (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    if (pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  // 4. merge every request's prefix segments and tail by log-sum-exp
+  return pkv::launch_lse_merge(out, out_lse, part_out, part_lse, c.splits + 1, bh, head_dim, st) ==
+                 cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

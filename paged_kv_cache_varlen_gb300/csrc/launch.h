@@ -39,6 +39,14 @@ struct AttnParams {
   float* ws_lse;              // [B][num_parts][H]
   int32_t* ws_cnt;            // [B][H] arrival counters, zero between calls
   int32_t* status;
+  // shared-prefix (cascade) pass of the prefill kernel: every query of a
+  // "request" (a prefix group) sees all seq_len keys, no causal mask; the
+  // keys are cut into at most kv_splits segments, segment s writing its
+  // normalised partial to out + s * split_out_stride and its lse to
+  // out_lse + s * split_lse_stride
+  int32_t prefix_mode;        // 0: ordinary causal prefill
+  int32_t kv_splits;
+  int64_t split_out_stride, split_lse_stride;
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
@@ -53,6 +61,11 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaSt
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle.
 // K/V pages are gathered through p.kv_pool.
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream);
+
+// Cascade preparation: part_lse[0 .. n_lse) = -inf and tail_cu[i] = i for
+// i <= num_seqs.
+cudaError_t launch_cascade_prepare(float* part_lse, int64_t n_lse, int32_t* tail_cu,
+                                   int32_t num_seqs, cudaStream_t stream);
 
 // Whole-block copies in the pool; block_vecs = 16-byte vectors in one
 // block of one half (K or V).

@@ -117,7 +117,21 @@ struct Bars {
 
 struct PrefillItem {
   int req, kvh, j0, j1, t0, qlen, L, kv_end, n_tiles;
+  int jb;   // first key tile of the item (a key segment in prefix mode)
+  int seg;  // key segment (prefix mode), else 0
 };
+
+// Prefix mode: the keys of a prefix of L tokens are cut into segments of
+// tiles_per_segment tiles; segment_count of them are non-empty.
+__device__ __forceinline__ int prefix_tiles_per_segment(int L, int splits) {
+  const int t = (L + kBN - 1) / kBN;
+  return (t + splits - 1) / splits;
+}
+__device__ __forceinline__ int prefix_segment_count(int L, int splits) {
+  const int t = (L + kBN - 1) / kBN;
+  const int tps = prefix_tiles_per_segment(L, splits);
+  return tps > 0 ? (t + tps - 1) / tps : 0;
+}
 
 // Work units (pairs of query tiles) of request r (0 for decode requests);
 // bad lengths flagged by CTA 0. QP = queries per unit.
@@ -128,6 +142,15 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP,
     return 0;
   }
   const int32_t qlen = t1 - t0;
+  if (p.prefix_mode) {  // a prefix group: qlen queries, all seeing L keys
+    const int32_t L = __ldg(p.seq_lens + r);
+    if (qlen > p.max_query_len || L < 0 || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
+      if (flag) set_status(p.status, PKV_DEV_BAD_LENGTHS);
+      return 0;
+    }
+    if (qlen < 1 || L == 0) return 0;
+    return ((qlen + QP - 1) / QP) * prefix_segment_count(L, p.kv_splits);
+  }
   if (qlen < 2) return 0;  // decode requests run on the decode kernel
   const int32_t L = __ldg(p.seq_lens + r);
   if (qlen > p.max_query_len || L < qlen || L > p.max_seq_len ||
@@ -186,11 +209,25 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
   d.qlen = __ldg(p.cu_seqlens + lo + 1) - d.t0;
   d.L = __ldg(p.seq_lens + lo);
   const int ntq = (d.qlen + QP - 1) / QP;
+  if (p.prefix_mode) {
+    const int segs = prefix_segment_count(d.L, p.kv_splits);
+    const int tps = prefix_tiles_per_segment(d.L, p.kv_splits);
+    const int local = u - pref[lo];
+    d.seg = local % segs;
+    d.j0 = (local / segs) * QP;
+    d.j1 = min(d.qlen, d.j0 + QP);
+    d.kv_end = d.L;  // every query sees the whole prefix
+    d.jb = d.seg * tps;
+    d.n_tiles = min((d.L + kBN - 1) / kBN, d.jb + tps) - d.jb;
+    return d;
+  }
   const int qt = ntq - 1 - (u - pref[lo]);  // later (heavier) units first
   d.j0 = qt * QP;
   d.j1 = min(d.qlen, d.j0 + QP);
   d.kv_end = d.L - d.qlen + d.j1;  // keys [0, kv_end) are needed
   d.n_tiles = (d.kv_end + kBN - 1) / kBN;
+  d.jb = 0;
+  d.seg = 0;
   return d;
 }
 
@@ -296,8 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t head_off = (int64_t)d.kvh * D * 2 + pc * 16;
       int32_t ids = -1;
       for (int j = 0; j < d.n_tiles; ++j, ++gt) {
+        const int jj = d.jb + j;  // key tile
         if ((j & 3) == 0) {  // block ids of the next 4 tiles, one 16-key sub-block per lane
-          const int key = (j * (kBN / kSub) + lane) * kSub;
+          const int key = (jj * (kBN / kSub) + lane) * kSub;
           ids = (key < d.kv_end) ? __ldg(bt + key / p.block_size) : -1;
         }
         // byte offset in the K half of the pool of each sub-block's first row
@@ -306,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int sb = 0; sb < kBN / kSub; ++sb) {
           const int32_t id = __shfl_sync(kFullMask, ids, (j & 3) * (kBN / kSub) + sb);
-          const int key = j * kBN + sb * kSub;
+          const int key = jj * kBN + sb * kSub;
           sub_off[sb] = -1;
           if (key < d.kv_end) {
             if (id < 0 || id >= p.num_blocks)
@@ -332,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < NIT; ++i) {
             const int k = pk0 + KSTEP * i;
             const int sb = (KSTEP * i) / kSub;
-            const bool valid = sub_off[sb] >= 0 && j * kBN + k < d.kv_end;
+            const bool valid = sub_off[sb] >= 0 && jj * kBN + k < d.kv_end;
             const uint8_t* src =
                 valid ? pool + base + sub_off[sb] + (int64_t)(k % kSub) * row_bytes : pool;
             cp_async_16(dst0 + k * 128 + ((pcc ^ (uint32_t)(k & 7)) << 4), src, valid ? 16u : 0u);
@@ -460,14 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PrefillItem d = prefill_item(p, pref, QP, it);
       const int qj = d.j0 + x * QT + rq;
       const bool row_valid = qj < d.j1;
-      const int pos = row_valid ? (d.L - d.qlen + qj) : (d.kv_end - 1);
+      const int pos = (row_valid && !p.prefix_mode) ? (d.L - d.qlen + qj) : (d.kv_end - 1);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < d.n_tiles; ++j) {
         const int gg = gt + j;
         ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->s_full[x]), gg & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
-        const int lim = pos - j * kBN;  // keys c <= lim of this tile are visible
+        const int lim = pos - (d.jb + j) * kBN;  // keys c <= lim of this tile are visible
         float alpha = 1.f, rs;
         bool resc;
         if (__all_sync(kFullMask, lim >= kBN - 1)) {
@@ -595,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* orow = p.out + ((int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g) * D;
+      float* orow = p.out + d.seg * p.split_out_stride +
+                    ((int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
@@ -610,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid && p.out_lse)
-        p.out_lse[(int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g] =
+        p.out_lse[d.seg * p.split_lse_stride + (int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g] =
             (m + fast_log2(l)) * kLn2;
       tc_fence_before();
       mbar_arrive(smem_addr(&bars->o_free[x]));  // the MMA may overwrite O_x now
@@ -647,7 +686,8 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cuda
   if (e != cudaSuccess) return e;
   const int G = p.num_heads / p.num_kv_heads;
   const int QP = kQT * (kBM / G);
-  const int64_t bound = (int64_t)p.num_seqs * ((p.max_query_len + QP - 1) / QP) * p.num_kv_heads;
+  const int64_t bound = (int64_t)p.num_seqs * ((p.max_query_len + QP - 1) / QP) * p.num_kv_heads *
+                        (p.prefix_mode ? p.kv_splits : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(bound < sms ? bound : sms));  // one CTA per SM (TMEM, smem)
   cfg.blockDim = dim3(kThreads);

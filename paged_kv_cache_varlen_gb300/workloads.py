@@ -327,6 +327,51 @@ CONFIGS = {
 }
 
 
+def cascade_inputs(w: Workload, groups) -> dict:
+    """Inputs of the shared-prefix (cascade) call for a workload whose
+    requests share copy-on-write prefixes: ``groups`` lists (first request,
+    count, prefix tokens), contiguous and in order; requests after the last
+    group have no prefix. Returns the group starts, prefix lengths and
+    tables, and every request's tail table (its blocks after the prefix) and
+    tail length, as int32 numpy arrays, plus the maxima the call takes."""
+    bs = w.block_size
+    starts = [0]
+    for first, count, _ in groups:
+        assert first == starts[-1], "groups must be contiguous and start at request 0"
+        starts.append(first + count)
+    prefix_of = np.zeros(w.num_seqs, dtype=np.int64)
+    for first, count, ptok in groups:
+        assert ptok % bs == 0
+        prefix_of[first:first + count] = ptok
+    max_pb = max([p // bs for _, _, p in groups] + [1])
+    ptables = np.full((max(len(groups), 1), max_pb), -1, dtype=np.int32)
+    for gi, (first, count, ptok) in enumerate(groups):
+        ptables[gi, :ptok // bs] = w.block_table[first, :ptok // bs]
+        assert (w.block_table[first:first + count, :ptok // bs] == ptables[gi, :ptok // bs]).all()
+    tail_lens = (w.seq_lens - prefix_of).astype(np.int32)
+    ttables = np.full((w.num_seqs, w.max_blocks), -1, dtype=np.int32)
+    for i in range(w.num_seqs):
+        nb_i = -(-int(tail_lens[i]) // bs)
+        off = int(prefix_of[i]) // bs
+        ttables[i, :nb_i] = w.block_table[i, off:off + nb_i]
+    return {
+        "group_starts": np.array(starts, dtype=np.int32),
+        "prefix_lens": np.array([p for _, _, p in groups] or [0], dtype=np.int32)[:len(groups)],
+        "prefix_tables": ptables[:len(groups)] if groups else ptables[:0],
+        "max_group_size": max([c for _, c, _ in groups] + [1]),
+        "max_prefix_len": max([p for _, _, p in groups] + [0]),
+        "tail_tables": ttables,
+        "tail_lens": tail_lens,
+        "max_tail_len": int(tail_lens.max()),
+    }
+
+
+def prefix_groups(w: Workload) -> list:
+    """The (first request, count, prefix tokens) groups of a prefix_shared workload."""
+    pg, g, ptok = w.meta["per_group"], w.meta["groups"], w.meta["prefix_tokens"]
+    return [(k * pg, pg, ptok) for k in range(g)]
+
+
 def permute_requests(w: Workload, order) -> Workload:
     """The same requests in another order (cu_seqlens, tables and tokens
     follow); the pool is unchanged."""
