@@ -79,7 +79,7 @@ def tensor_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("decode.cu", "merge.cu", "common.cuh"):
+    for f in ("decode_mma.cu", "merge.cu", "common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_varlen_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

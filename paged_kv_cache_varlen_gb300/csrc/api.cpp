@@ -56,6 +56,21 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 4-D bf16 tensor [d3][d2][d1][d0] (d0 contiguous) with byte strides s1..s3.
+bool encode_4d(CUtensorMap* map, const void* base, const uint64_t (&dims)[4],
+               const uint64_t (&strides)[3], const uint32_t (&box)[4],
+               CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t s[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, s, b, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Partition length and count for query_len == 1 requests.
 bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps, int32_t* np) {
   if (partition_size < -1) return false;
@@ -263,12 +278,15 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
 
   const uint64_t D = (uint64_t)head_dim;
   const uint64_t pool_rows = (uint64_t)2 * num_blocks * block_size;
-  // decode: a 16-key box of whole rows, no swizzle
+  // decode: a 16-key box of whole rows (as 128-byte halves, swizzled for
+  // conflict-free ldmatrix)
   CUtensorMap kv_rows;
-  if (!encode_3d(&kv_rows, kv_pool, D, num_kv_heads, pool_rows, D * 2, (uint64_t)num_kv_heads * D * 2,
-                 (uint32_t)D, 1, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+  const uint64_t dims[4] = {64, D / 64, (uint64_t)num_kv_heads, pool_rows};
+  const uint64_t strides[3] = {128, D * 2, (uint64_t)num_kv_heads * D * 2};
+  const uint32_t box[4] = {64, (uint32_t)(D / 64), 1, 16};
+  if (!encode_4d(&kv_rows, kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return PKV_ERR_CUDA;
-  if (pkv::launch_decode(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (pkv::launch_decode_mma(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
 
   if (max_query_len > 1) {
     CUtensorMap q_map;

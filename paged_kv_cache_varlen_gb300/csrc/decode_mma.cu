@@ -1,0 +1,482 @@
+// decode_mma.cu -- paged attention for query_len == 1 requests (decode),
+// with the two products of each 16-token chunk on the warp-level tensor-core
+// path (mma.sync m16n8k16: bf16 operands, fp32 accumulation).
+//
+// Method (sources as cited in include/pkv.h):
+//   page 1 §04: GQA, kv_head = q_head / (num_heads / num_kv_heads); decode
+//     is a matrix-vector product bound by moving the KV cache from HBM.
+//   page 1 §02 / page 2 (PagedAttention deep-dive): block_table maps the
+//     request's logical blocks to physical pool blocks.
+//   page 2 step 4: causal mask; the single query sits at position
+//     seq_len - 1 and sees every cached key, including its own.
+//   page 3 §3.4: fused, exact attention (online softmax on chip).
+//   page 1 §07: long contexts split into partitions merged by log-sum-exp.
+//
+// Why tensor cores here: on CUDA cores a GQA group of 4 heads costs ~1024
+// fp32 FMAs per (token, KV head) plus bf16 unpacking and shuffles for 512
+// bytes of K and V; measured on GB300 that arithmetic, not HBM, bound the
+// kernel (issue ~46 % active, ~52 warp instructions per token and KV head).
+// The group's query heads form the 16 rows of an m16n8k16 tile, so each
+// chunk's QK^T and PV are ~48 MMAs per warp instead, and the kernel is left
+// to stream K/V.
+//
+// GB300 design (the pipeline is the one of the CUDA-core decode kernel):
+//   * one CTA = (request, KV head, subgroup of up to 16 query heads,
+//     partition); each K/V byte of a partition is read from HBM once;
+//   * 4 warps, each with SPW private slots; a slot holds one 16-token chunk
+//     of K and of V for this KV head, fetched by one TMA load each (box of
+//     16 rows x head_dim, 128-byte swizzle so that ldmatrix reads of 8 rows
+//     hit different banks) and completed on the slot's mbarrier;
+//   * S = Q K^T: Q is held as A fragments (rows = heads, zero padded), K
+//     rows come in by ldmatrix as B fragments; online softmax in the exp2
+//     domain with lazy rescaling (the running maximum moves only when a score
+//     exceeds it by more than 8); P goes straight from the accumulator
+//     registers into A fragments as a bf16 high part and a bf16 remainder
+//     (p ~= hi + lo to ~2^-16, as the prefill kernel does), and O += P V
+//     with V rows from ldmatrix.trans; V rows of tokens past the context are
+//     zeroed first (P is 0 there, and 0 * NaN is not);
+//   * end: warps merge through shared memory; a split request's partitions
+//     are merged by the last partition CTA to finish, as in the CUDA-core
+//     kernel; programmatic dependent launch as well.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kChunk = 16;  // tokens per TMA box and per pipeline stage
+constexpr int kWarps = 4;
+constexpr int kRows = 16;   // MMA rows: query heads of the subgroup, zero padded
+constexpr float kRescaleThreshold = 8.f;
+constexpr uint32_t kFull = 0xffffffffu;
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Byte offset of 16-byte unit `unit` of row `token` in a 16-row x D tile
+// written by TMA with 128-byte swizzle (tile base 1024-byte aligned): row
+// `token` is D/64 consecutive 128-byte lines; inside line q the unit u sits
+// at u ^ (q % 8).
+template <int D>
+__device__ __forceinline__ uint32_t swz(int token, int unit) {
+  const int line = token * (D / 64) + (unit >> 3);
+  return (uint32_t)(line * 128 + (((unit & 7) ^ (line & 7)) << 4));
+}
+
+template <int D, int SPW, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
+  constexpr int KS = D / 16;            // k-steps of QK^T
+  constexpr int NT = D / 8;             // n-tiles of PV
+  constexpr int HALF = kChunk * D * 2;  // bytes of the K (or V) rows of a chunk
+  constexpr int SLOT = 2 * HALF;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* slots = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * SPW * SLOT);
+  int* flag = reinterpret_cast<int*>(bars + kWarps * SPW);
+
+  // Everything below may read the pool the preceding KV write produces.
+  griddep_wait();
+  griddep_launch_dependents();
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int group = p.num_heads / p.num_kv_heads;
+  const int nsub = (group + kRows - 1) / kRows;
+  const int kvh = blockIdx.x / nsub;
+  const int sub = blockIdx.x - kvh * nsub;
+  const int rows = min(kRows, group - sub * kRows);  // query heads of this CTA
+  const int h0 = kvh * group + sub * kRows;
+  const int part = blockIdx.y;
+  const int i = blockIdx.z;
+  const bool leader = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+
+  const int32_t t0 = p.cu_seqlens[i];
+  const int32_t t1 = p.cu_seqlens[i + 1];
+  if (t0 < 0 || t1 < t0 || t1 > p.num_tokens) {
+    if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
+    return;
+  }
+  if (t1 - t0 != 1) return;  // not a decode request
+  const int32_t L = p.seq_lens[i];
+  if (L < 1 || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
+    if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
+    return;
+  }
+  const int32_t kbeg = part * p.part_size;
+  if (kbeg >= L) return;
+  const int32_t kend = min(L, kbeg + p.part_size);
+  const int nchunks = (kend - kbeg + kChunk - 1) / kChunk;
+  const int my_chunks = (nchunks - warp + kWarps - 1) / kWarps;
+
+  if (lane == 0) {
+    for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[warp * SPW + s]), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&kv_map);
+  __syncwarp();
+
+  const int32_t* bt = p.block_table + (int64_t)i * p.max_blocks;
+  // lane j of the warp caches the block id of the warp's chunk (kb + j)
+  auto load_ids = [&](int kb) -> int32_t {
+    const int k = kb + lane;
+    if (k >= my_chunks) return -1;
+    const int c = warp + k * kWarps;
+    return __ldg(bt + (kbeg + c * kChunk) / p.block_size);
+  };
+  const int32_t nrows = p.num_blocks * p.block_size;
+  auto issue = [&](int k, int32_t id) {  // lane 0 only
+    const int slot = k % SPW;
+    const uint32_t bar = smem_addr(&bars[warp * SPW + slot]);
+    if (id < 0 || id >= p.num_blocks) {
+      set_status(p.status, PKV_DEV_BAD_BLOCK);
+      mbar_arrive(bar);  // no bytes: the chunk is skipped (masked)
+      return;
+    }
+    const uint32_t dst = smem_addr(slots + (warp * SPW + slot) * SLOT);
+    const int key0 = kbeg + (warp + k * kWarps) * kChunk;
+    const int32_t row = id * p.block_size + key0 % p.block_size;
+    mbar_arrive_expect_tx(bar, SLOT);
+    tma_load_4d(dst, &kv_map, bar, 0, 0, kvh, row);
+    tma_load_4d(dst + HALF, &kv_map, bar, 0, 0, kvh, row + nrows);
+  };
+
+  int32_t ids_cur = load_ids(0);
+  int32_t ids_next = load_ids(32);
+  int issued = 0;
+  for (int k = 0; k < SPW && k < my_chunks; ++k) {
+    const int32_t id = __shfl_sync(kFull, ids_cur, k);
+    if (lane == 0) issue(k, id);
+    ++issued;
+  }
+
+  // Q of the subgroup as A fragments: row r = lane / 4 (and r + 8), columns
+  // (lane % 4) * 2 + {0, 1} (and + 8) of every 16-wide k-step; rows past the
+  // subgroup are zero.
+  const int r = lane >> 2;
+  const int cq = (lane & 3) * 2;
+  uint32_t qa[KS][4];
+  {
+    const uint16_t* q_r = p.q + ((int64_t)t0 * p.num_heads + h0 + r) * D + cq;
+    const bool lo_ok = r < rows, hi_ok = r + 8 < rows;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint16_t* qk = q_r + ks * 16;
+      qa[ks][0] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk)) : 0u;
+      qa[ks][1] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8 * D)) : 0u;
+      qa[ks][2] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8)) : 0u;
+      qa[ks][3] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8 * D + 8)) : 0u;
+    }
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // running maxima of rows r, r + 8 (log2 units)
+  float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+  const float sl2 = p.scale_log2;
+
+  // ldmatrix lane addresses inside a tile: K (x4: tokens 0-7 / 8-15 x the
+  // two 8-wide halves of a k-step) and V (x4.trans: tokens 0-7 / 8-15 x two
+  // 8-wide n-tiles)
+  const int mi = lane >> 3;
+  const int k_tok = ((mi >> 1) << 3) + (lane & 7), k_unit = mi & 1;
+  const int v_tok = ((mi & 1) << 3) + (lane & 7), v_unit = mi >> 1;
+
+  int kb = 0;
+  int consumed = 0;
+  for (int k = 0; k < my_chunks; ++k) {
+    if (k - kb == 32) {
+      kb += 32;
+      ids_cur = ids_next;
+      ids_next = load_ids(kb + 32);
+    }
+    const int slot = k % SPW;
+    const bool ok =
+        __all_sync(kFull, mbar_wait(smem_addr(&bars[warp * SPW + slot]), (k / SPW) & 1, p.status));
+    if (!ok) break;
+    consumed = k + 1;
+    const int32_t id = __shfl_sync(kFull, ids_cur, k - kb);
+    const bool chunk_ok = (id >= 0 && id < p.num_blocks);
+    const int key0 = kbeg + (warp + k * kWarps) * kChunk;
+    const int nvalid = chunk_ok ? min(kChunk, kend - key0) : 0;
+    uint8_t* kbase = slots + (warp * SPW + slot) * SLOT;
+    uint8_t* vbase = kbase + HALF;
+    if (nvalid < kChunk) {
+      // rows past the context may hold anything, NaN included: zero those V
+      // rows (their P is 0, and 0 * NaN would poison O)
+      for (int e = lane; e < (kChunk - nvalid) * (D / 8); e += 32) {
+        const int tok = nvalid + e / (D / 8);
+        *reinterpret_cast<uint4*>(vbase + swz<D>(tok, e % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    const uint32_t ka = smem_addr(kbase), va = smem_addr(vbase);
+
+    // ---- S = Q K^T (two 8-token n-tiles)
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b[4];
+      ldsm_x4(ka + swz<D>(k_tok, ks * 2 + k_unit), b);
+      mma_16816(s[0], qa[ks], b[0], b[1]);
+      mma_16816(s[1], qa[ks], b[2], b[3]);
+    }
+    // ---- mask, chunk maxima (the 4 lanes of a quad share a row)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (nt * 8 + cq + j >= nvalid) {
+          s[nt][j] = -INFINITY;
+          s[nt][2 + j] = -INFINITY;
+        }
+        mx0 = fmaxf(mx0, s[nt][j]);
+        mx1 = fmaxf(mx1, s[nt][2 + j]);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+    const float n0 = fmaxf(m0, __fmul_rn(mx0, sl2)), n1 = fmaxf(m1, __fmul_rn(mx1, sl2));
+    const bool r0 = n0 > m0 + kRescaleThreshold, r1 = n1 > m1 + kRescaleThreshold;
+    if (__any_sync(kFull, r0 || r1)) {
+      const float a0 = r0 ? fast_exp2(m0 - n0) : 1.f;  // 0 when m was -inf
+      const float a1 = r1 ? fast_exp2(m1 - n1) : 1.f;
+      if (r0) m0 = n0;
+      if (r1) m1 = n1;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= a0;
+        o[nt][1] *= a0;
+        o[nt][2] *= a1;
+        o[nt][3] *= a1;
+      }
+    }
+    // ---- P = 2^(s * scale * log2 e - m), as bf16 hi + lo A fragments
+    const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        // the product rounded exactly as for the maximum, so that the
+        // largest score gives p = 1 exactly
+        pr[nt][j] = fast_exp2(__fmul_rn(s[nt][j], sl2) - mu0);
+        pr[nt][2 + j] = fast_exp2(__fmul_rn(s[nt][2 + j], sl2) - mu1);
+      }
+    l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    uint32_t ah[4], al[4];
+    ah[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    ah[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    ah[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    ah[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    al[0] = pack_bf16x2(pr[0][0] - bf16_lo(ah[0]), pr[0][1] - bf16_hi(ah[0]));
+    al[1] = pack_bf16x2(pr[0][2] - bf16_lo(ah[1]), pr[0][3] - bf16_hi(ah[1]));
+    al[2] = pack_bf16x2(pr[1][0] - bf16_lo(ah[2]), pr[1][1] - bf16_hi(ah[2]));
+    al[3] = pack_bf16x2(pr[1][2] - bf16_lo(ah[3]), pr[1][3] - bf16_hi(ah[3]));
+    // ---- O += P V (two n-tiles per ldmatrix)
+#pragma unroll
+    for (int n2 = 0; n2 < NT / 2; ++n2) {
+      uint32_t b[4];
+      ldsm_x4_trans(va + swz<D>(v_tok, n2 * 2 + v_unit), b);
+      mma_16816(o[2 * n2], ah, b[0], b[1]);
+      mma_16816(o[2 * n2], al, b[0], b[1]);
+      mma_16816(o[2 * n2 + 1], ah, b[2], b[3]);
+      mma_16816(o[2 * n2 + 1], al, b[2], b[3]);
+    }
+    __syncwarp();
+    const int kn = k + SPW;
+    if (kn < my_chunks) {
+      const int32_t idn = (kn - kb < 32) ? __shfl_sync(kFull, ids_cur, kn - kb)
+                                         : __shfl_sync(kFull, ids_next, kn - kb - 32);
+      if (lane == 0) {
+        fence_proxy_async_smem();  // our reads and writes of the slot precede the refill
+        issue(kn, idn);
+      }
+      ++issued;
+    }
+  }
+  // After an abandoned wait, let this warp's copies in flight land before the
+  // CTA leaves (bounded as well).
+  for (int k = consumed; k < issued; ++k)
+    mbar_wait(smem_addr(&bars[warp * SPW + (k % SPW)]), (k / SPW) & 1, nullptr);
+
+  // the quad's lanes hold a row's sum in four pieces
+  l0 += __shfl_xor_sync(kFull, l0, 1);
+  l0 += __shfl_xor_sync(kFull, l0, 2);
+  l1 += __shfl_xor_sync(kFull, l1, 1);
+  l1 += __shfl_xor_sync(kFull, l1, 2);
+
+  __syncthreads();  // every warp is done with its slots: reuse them
+  float* red_o = reinterpret_cast<float*>(smem);       // [kWarps][kRows][D]
+  float* red_ml = red_o + kWarps * kRows * D;          // [kWarps][kRows][2]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float* dst = red_o + (warp * kRows + r) * D + nt * 8 + cq;
+    dst[0] = o[nt][0];
+    dst[1] = o[nt][1];
+    dst[8 * D] = o[nt][2];
+    dst[8 * D + 1] = o[nt][3];
+  }
+  if ((lane & 3) == 0) {
+    red_ml[(warp * kRows + r) * 2] = m0;
+    red_ml[(warp * kRows + r) * 2 + 1] = l0;
+    red_ml[(warp * kRows + r + 8) * 2] = m1;
+    red_ml[(warp * kRows + r + 8) * 2 + 1] = l1;
+  }
+  __syncthreads();
+
+  const int parts_i = (L + p.part_size - 1) / p.part_size;
+  for (int idx = threadIdx.x; idx < rows * D; idx += kWarps * 32) {
+    const int g = idx / D;
+    const int d = idx - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[(w * kRows + g) * 2]);
+    float wsum = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = red_ml[(w * kRows + g) * 2];
+      if (mw == -INFINITY) continue;
+      const float a = fast_exp2(mw - M);
+      wsum += a * red_ml[(w * kRows + g) * 2 + 1];
+      acc += a * red_o[(w * kRows + g) * D + d];
+    }
+    const float val = wsum > 0.f ? acc / wsum : 0.f;
+    const float lse = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
+    const int h = h0 + g;
+    if (parts_i == 1) {
+      p.out[((int64_t)t0 * p.num_heads + h) * D + d] = val;
+      if (d == 0 && p.out_lse) p.out_lse[(int64_t)t0 * p.num_heads + h] = lse;
+    } else {
+      const int64_t rr = ((int64_t)i * p.num_parts + part) * p.num_heads + h;
+      p.ws_out[rr * D + d] = val;
+      if (d == 0) p.ws_lse[rr] = lse;
+    }
+  }
+  if (parts_i == 1) return;
+
+  // ---- split request: the last partition CTA of (request, head subgroup) merges
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // publish this CTA's partial before counting it
+    const int old = atomicAdd(&p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x], 1);
+    *flag = (old == parts_i - 1);
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();  // see every other partition's partial
+  float* mg = red_ml;  // [rows] maxima of the partial lse (reuses shared memory)
+  const int64_t row0 = (int64_t)i * p.num_parts * p.num_heads;
+  for (int g = warp; g < rows; g += kWarps) {
+    float M = -INFINITY;
+    for (int pp = lane; pp < parts_i; pp += 32)
+      M = fmaxf(M, __ldcg(p.ws_lse + row0 + (int64_t)pp * p.num_heads + h0 + g));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    if (lane == 0) mg[g] = M;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * D / 4; idx += kWarps * 32) {
+    const int g = idx / (D / 4);
+    const int d4 = idx - g * (D / 4);
+    const float M = mg[g];
+    const int h = h0 + g;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int pp = 0; pp < parts_i; ++pp) {
+        const int64_t rr = row0 + (int64_t)pp * p.num_heads + h;
+        const float w = fast_exp2((__ldcg(p.ws_lse + rr) - M) * kLog2e);  // 0 for an empty part
+        const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.ws_out + rr * D) + d4);
+        wsum += w;
+        acc.x += w * ov.x;
+        acc.y += w * ov.y;
+        acc.z += w * ov.z;
+        acc.w += w * ov.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    reinterpret_cast<float4*>(p.out + ((int64_t)t0 * p.num_heads + h) * D)[d4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (d4 == 0 && p.out_lse)
+      p.out_lse[(int64_t)t0 * p.num_heads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  }
+  if (threadIdx.x == 0) p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x] = 0;  // ready for reuse
+}
+
+#ifndef PKV_DECODE_MMA_MINB
+#define PKV_DECODE_MMA_MINB 3
+#endif
+#ifndef PKV_DECODE_MMA_SPW
+#define PKV_DECODE_MMA_SPW 2
+#endif
+
+template <int D>
+cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
+                                cudaStream_t stream) {
+  constexpr int SPW = PKV_DECODE_MMA_SPW, MINB = PKV_DECODE_MMA_MINB;
+  constexpr size_t SLOT = 2 * kChunk * D * 2;
+  const size_t smem = 1024 + kWarps * SPW * SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
+  auto kernel = decode_mma_kernel<D, SPW, MINB>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int group = p.num_heads / p.num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_kv_heads * ((group + kRows - 1) / kRows), p.num_parts, p.num_seqs);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, kv_map, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream) {
+  if (p.head_dim == 128) return launch_decode_mma_d<128>(p, kv_map, stream);
+  if (p.head_dim == 64) return launch_decode_mma_d<64>(p, kv_map, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -51,11 +51,13 @@ struct AttnParams {
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 
-// Decode kernel (query_len == 1 requests), CUDA cores, TMA-staged pages,
-// split-KV partitions merged in-kernel by the last partition CTA.
-// `kv_map` views the pool as [2*NB*BS rows][Hkv][D] with a box of
-// {D, 1, 16}.
-cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kv_map, cudaStream_t stream);
+// Decode kernel (query_len == 1 requests): TMA-staged pages, QK^T and PV on
+// the warp-level tensor cores (mma.sync), split-KV partitions merged
+// in-kernel by the last partition CTA. `kv_map` views the pool as
+// [2*NB*BS rows][Hkv][D/64][64] with a box of {64, D/64, 1, 16} and 128-byte
+// swizzle. Up to 16 query heads per CTA.
+cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
+                              cudaStream_t stream);
 
 // Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle.
