@@ -264,6 +264,10 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.ws_out = nullptr;
   p.ws_lse = nullptr;
   p.ws_cnt = nullptr;
+  // the decode kernel takes requests of up to 32 (query, head) rows: two
+  // subgroups of its 16-row MMA tiles
+  p.decode_max_q = 32 / group > 1 ? 32 / group : 1;
+  p.decode_max_rows = (max_query_len < p.decode_max_q ? max_query_len : p.decode_max_q) * group;
   p.prefix_mode = 0;
   p.kv_splits = 1;
   p.split_out_stride = 0;
@@ -288,7 +292,7 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
     return PKV_ERR_CUDA;
   if (pkv::launch_decode_mma(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
 
-  if (max_query_len > 1) {
+  if (max_query_len > p.decode_max_q) {
     CUtensorMap q_map;
     if (!encode_3d(&q_map, q, D, num_heads, num_tokens, D * 2, (uint64_t)num_heads * D * 2, 64,
                    (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
@@ -404,6 +408,8 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.ws_lse = nullptr;
     p.ws_cnt = nullptr;
     p.status = dev_status;
+    p.decode_max_q = 0;  // the prefix pass takes every group
+    p.decode_max_rows = 0;
     p.prefix_mode = 1;
     p.kv_splits = c.splits;
     p.split_out_stride = bh * head_dim;

@@ -105,12 +105,13 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  // MMA rows of a request: (query j, head g) pairs, j-major, cut into
+  // subgroups of 16 rows; one query per request (decode) makes the rows the
+  // heads of the GQA group
   const int group = p.num_heads / p.num_kv_heads;
-  const int nsub = (group + kRows - 1) / kRows;
+  const int nsub = (p.decode_max_rows + kRows - 1) / kRows;
   const int kvh = blockIdx.x / nsub;
   const int sub = blockIdx.x - kvh * nsub;
-  const int rows = min(kRows, group - sub * kRows);  // query heads of this CTA
-  const int h0 = kvh * group + sub * kRows;
   const int part = blockIdx.y;
   const int i = blockIdx.z;
   const bool leader = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
@@ -121,15 +122,22 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return;
   }
-  if (t1 - t0 != 1) return;  // not a decode request
+  const int32_t qlen = t1 - t0;
+  if (qlen < 1 || qlen > p.decode_max_q) return;  // longer requests run on the prefill kernel
+  const int row0 = sub * kRows;
+  if (row0 >= qlen * group) return;  // no row of this request in the subgroup
+  const int rows = min(kRows, qlen * group - row0);  // rows of this CTA
   const int32_t L = p.seq_lens[i];
-  if (L < 1 || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
+  if (L < qlen || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
     if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return;
   }
-  const int32_t kbeg = part * p.part_size;
+  // several queries (a verification step): one partition over every key,
+  // with the causal limit per row; one query: the split-KV partitions
+  if (qlen > 1 && part > 0) return;
+  const int32_t kbeg = qlen > 1 ? 0 : part * p.part_size;
   if (kbeg >= L) return;
-  const int32_t kend = min(L, kbeg + p.part_size);
+  const int32_t kend = qlen > 1 ? L : min(L, kbeg + p.part_size);
   const int nchunks = (kend - kbeg + kChunk - 1) / kChunk;
   const int my_chunks = (nchunks - warp + kWarps - 1) / kWarps;
 
@@ -179,19 +187,27 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // subgroup are zero.
   const int r = lane >> 2;
   const int cq = (lane & 3) * 2;
+  // row -> (query, head): the query's token and the causal key limit
+  auto row_token = [&](int rr) { return t0 + (row0 + rr) / group; };
+  auto row_head = [&](int rr) { return kvh * group + (row0 + rr) % group; };
+  auto row_limit = [&](int rr) {  // keys < limit are visible to the row
+    return rr < rows ? min(kend, L - qlen + (row0 + rr) / group + 1) : 0;
+  };
   uint32_t qa[KS][4];
   {
-    const uint16_t* q_r = p.q + ((int64_t)t0 * p.num_heads + h0 + r) * D + cq;
     const bool lo_ok = r < rows, hi_ok = r + 8 < rows;
+    const uint16_t* q_lo = p.q + ((int64_t)row_token(r) * p.num_heads + row_head(r)) * D + cq;
+    const uint16_t* q_hi =
+        p.q + ((int64_t)row_token(r + 8) * p.num_heads + row_head(r + 8)) * D + cq;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const uint16_t* qk = q_r + ks * 16;
-      qa[ks][0] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk)) : 0u;
-      qa[ks][1] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8 * D)) : 0u;
-      qa[ks][2] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8)) : 0u;
-      qa[ks][3] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qk + 8 * D + 8)) : 0u;
+      qa[ks][0] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(q_lo + ks * 16)) : 0u;
+      qa[ks][1] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(q_hi + ks * 16)) : 0u;
+      qa[ks][2] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(q_lo + ks * 16 + 8)) : 0u;
+      qa[ks][3] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(q_hi + ks * 16 + 8)) : 0u;
     }
   }
+  const int lim0 = row_limit(r), lim1 = row_limit(r + 8);
   float o[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
@@ -247,16 +263,16 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       mma_16816(s[0], qa[ks], b[0], b[1]);
       mma_16816(s[1], qa[ks], b[2], b[3]);
     }
-    // ---- mask, chunk maxima (the 4 lanes of a quad share a row)
+    // ---- mask (past the context, or after the row's own position), chunk
+    // maxima (the 4 lanes of a quad share a row)
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        if (nt * 8 + cq + j >= nvalid) {
-          s[nt][j] = -INFINITY;
-          s[nt][2 + j] = -INFINITY;
-        }
+        const int tok = nt * 8 + cq + j;
+        if (tok >= nvalid || key0 + tok >= lim0) s[nt][j] = -INFINITY;
+        if (tok >= nvalid || key0 + tok >= lim1) s[nt][2 + j] = -INFINITY;
         mx0 = fmaxf(mx0, s[nt][j]);
         mx1 = fmaxf(mx1, s[nt][2 + j]);
       }
@@ -356,7 +372,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   }
   __syncthreads();
 
-  const int parts_i = (L + p.part_size - 1) / p.part_size;
+  const int parts_i = qlen > 1 ? 1 : (L + p.part_size - 1) / p.part_size;
+  const int h0 = kvh * group + row0;  // one query: row g is head h0 + g
   for (int idx = threadIdx.x; idx < rows * D; idx += kWarps * 32) {
     const int g = idx / D;
     const int d = idx - g * D;
@@ -374,11 +391,12 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     }
     const float val = wsum > 0.f ? acc / wsum : 0.f;
     const float lse = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
-    const int h = h0 + g;
     if (parts_i == 1) {
-      p.out[((int64_t)t0 * p.num_heads + h) * D + d] = val;
-      if (d == 0 && p.out_lse) p.out_lse[(int64_t)t0 * p.num_heads + h] = lse;
+      const int64_t orow = (int64_t)row_token(g) * p.num_heads + row_head(g);
+      p.out[orow * D + d] = val;
+      if (d == 0 && p.out_lse) p.out_lse[orow] = lse;
     } else {
+      const int h = h0 + g;
       const int64_t rr = ((int64_t)i * p.num_parts + part) * p.num_heads + h;
       p.ws_out[rr * D + d] = val;
       if (d == 0) p.ws_lse[rr] = lse;
@@ -386,22 +404,25 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   }
   if (parts_i == 1) return;
 
-  // ---- split request: the last partition CTA of (request, head subgroup) merges
+  // ---- split request (one query): the last partition CTA of (request, head
+  // subgroup) merges; counters [request][KV head][subgroup of the heads]
+  const int nsub1 = (group + kRows - 1) / kRows;
+  int32_t* cnt = p.ws_cnt + ((int64_t)i * p.num_kv_heads + kvh) * nsub1 + sub;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // publish this CTA's partial before counting it
-    const int old = atomicAdd(&p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x], 1);
+    const int old = atomicAdd(cnt, 1);
     *flag = (old == parts_i - 1);
   }
   __syncthreads();
   if (!*flag) return;
   __threadfence();  // see every other partition's partial
   float* mg = red_ml;  // [rows] maxima of the partial lse (reuses shared memory)
-  const int64_t row0 = (int64_t)i * p.num_parts * p.num_heads;
+  const int64_t wrow0 = (int64_t)i * p.num_parts * p.num_heads;
   for (int g = warp; g < rows; g += kWarps) {
     float M = -INFINITY;
     for (int pp = lane; pp < parts_i; pp += 32)
-      M = fmaxf(M, __ldcg(p.ws_lse + row0 + (int64_t)pp * p.num_heads + h0 + g));
+      M = fmaxf(M, __ldcg(p.ws_lse + wrow0 + (int64_t)pp * p.num_heads + h0 + g));
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
     if (lane == 0) mg[g] = M;
@@ -417,7 +438,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     if (M != -INFINITY) {
 #pragma unroll 4
       for (int pp = 0; pp < parts_i; ++pp) {
-        const int64_t rr = row0 + (int64_t)pp * p.num_heads + h;
+        const int64_t rr = wrow0 + (int64_t)pp * p.num_heads + h;
         const float w = fast_exp2((__ldcg(p.ws_lse + rr) - M) * kLog2e);  // 0 for an empty part
         const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.ws_out + rr * D) + d4);
         wsum += w;
@@ -433,7 +454,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     if (d4 == 0 && p.out_lse)
       p.out_lse[(int64_t)t0 * p.num_heads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
   }
-  if (threadIdx.x == 0) p.ws_cnt[(int64_t)i * gridDim.x + blockIdx.x] = 0;  // ready for reuse
+  if (threadIdx.x == 0) *cnt = 0;  // ready for reuse
 }
 
 #ifndef PKV_DECODE_MMA_MINB
@@ -457,9 +478,9 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int group = p.num_heads / p.num_kv_heads;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_kv_heads * ((group + kRows - 1) / kRows), p.num_parts, p.num_seqs);
+  cfg.gridDim = dim3(p.num_kv_heads * ((p.decode_max_rows + kRows - 1) / kRows), p.num_parts,
+                     p.num_seqs);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -44,6 +44,10 @@ struct AttnParams {
   // keys are cut into at most kv_splits segments, segment s writing its
   // normalised partial to out + s * split_out_stride and its lse to
   // out_lse + s * split_lse_stride
+  // requests of 1 .. decode_max_q queries run on the decode kernel (its MMA
+  // rows are (query, head) pairs, at most decode_max_rows per request in the
+  // launch); longer ones on the prefill kernel
+  int32_t decode_max_q, decode_max_rows;
   int32_t prefix_mode;        // 0: ordinary causal prefill
   int32_t kv_splits;
   int64_t split_out_stride, split_lse_stride;

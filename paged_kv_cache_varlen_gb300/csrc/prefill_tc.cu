@@ -151,7 +151,7 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP,
     if (qlen < 1 || L == 0) return 0;
     return ((qlen + QP - 1) / QP) * prefix_segment_count(L, p.kv_splits);
   }
-  if (qlen < 2) return 0;  // decode requests run on the decode kernel
+  if (qlen <= p.decode_max_q) return 0;  // short requests run on the decode kernel
   const int32_t L = __ldg(p.seq_lens + r);
   if (qlen > p.max_query_len || L < qlen || L > p.max_seq_len ||
       L > p.max_blocks * p.block_size) {
