@@ -79,6 +79,22 @@ def test_short_query_chunks(oracle, qlens):
     _run_and_check(oracle, w)
 
 
+@pytest.mark.parametrize("H,Hkv,D", [(32, 8, 128), (32, 4, 128), (8, 8, 64), (32, 2, 128),
+                                     (32, 1, 64)])
+def test_verification_steps_around_the_decode_cutoff(oracle, H, Hkv, D):
+    """Requests of a few queries run on the decode kernel while their
+    (query, head) rows fit two 16-row MMA subgroups (q <= 32 / G), and on
+    the prefill kernel beyond: every q from 1 to one past the cutoff, over
+    prior contexts from empty to several blocks."""
+    G = H // Hkv
+    cut = max(1, 32 // G)
+    qlens = list(range(1, cut + 2))
+    prior = [(37 * k) % 300 for k in range(len(qlens))]
+    L = [p + q for p, q in zip(prior, qlens)]
+    w = wl.build("verify", L, qlens, H, Hkv, D, seed=260 + G + D)
+    _run_and_check(oracle, w)
+
+
 def test_full_prefill_without_prior_context(oracle):
     w = wl.build("fresh", [1, 2, 127, 128, 129, 600], [1, 2, 127, 128, 129, 600], 32, 8, 128,
                  seed=207)
