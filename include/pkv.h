@@ -87,13 +87,15 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
 /*
  * pkv_attention_workspace_size -- bytes of scratch that
  * pkv_paged_attention_varlen needs for these sizes and this partition_size
- * (0 when the call needs none). The caller allocates it (a 256-byte aligned
+ * (at least 256: the prefill kernel's work tickets; split-KV partials on top;
+ * 0 only for invalid sizes). The caller allocates it (a 256-byte aligned
  * device buffer at least this large) and ZERO-FILLS it once before its first
- * use (it holds per-request arrival counters of the split-KV merge). Every
- * call that completes without PKV_DEV_TIMEOUT leaves it zero-filled again,
- * so one workspace serves any number of calls on one stream; calls that may
- * run concurrently need separate workspaces. After a PKV_DEV_TIMEOUT, clear
- * it again before reuse.
+ * use (it holds per-request arrival counters of the split-KV merge and the
+ * counter from which prefill CTAs take their work items). Every call that
+ * completes without PKV_DEV_TIMEOUT leaves it zero-filled again, so one
+ * workspace serves any number of calls on one stream; calls that may run
+ * concurrently need separate workspaces. After a PKV_DEV_TIMEOUT, clear it
+ * again before reuse.
  */
 size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
                                     int32_t num_kv_heads, int32_t head_dim,
@@ -129,8 +131,8 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  *                > 0 = that many tokens, a multiple of 16. A split request's
  *                partitions are merged by log-sum-exp inside the same kernel
  *   workspace, workspace_bytes: scratch of at least
- *                pkv_attention_workspace_size(...) bytes (may be NULL when
- *                that size is 0)
+ *                pkv_attention_workspace_size(...) bytes, zero-filled before
+ *                its first use (see there)
  *
  * Query j of request i sits at position pos = seq_len_i - query_len_i + j
  * and attends to keys 0..pos (bottom-right causal alignment). Keys beyond

@@ -94,19 +94,24 @@ bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps,
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: partial outputs [B][P][H][D] fp32, partial lse [B][P][H] fp32,
-// arrival counters [B][H] int32 (zero between calls).
+// arrival counters [B][H] int32 (split-KV only), then the prefill work
+// tickets (256 bytes, always); counters and tickets are zero between calls.
+constexpr size_t kSchedBytes = 256;
+
 struct WorkspaceLayout {
-  size_t lse_off, cnt_off, total;
+  size_t lse_off, cnt_off, sched_off, total;
 };
 
 WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                                  int32_t nparts) {
-  WorkspaceLayout w{0, 0, 0};
-  if (nparts <= 1) return w;
-  const size_t rows = (size_t)num_seqs * nparts * num_heads;
-  w.lse_off = round_up(rows * head_dim * sizeof(float), 256);
-  w.cnt_off = w.lse_off + round_up(rows * sizeof(float), 256);
-  w.total = w.cnt_off + round_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+  WorkspaceLayout w{0, 0, 0, 0};
+  if (nparts > 1) {
+    const size_t rows = (size_t)num_seqs * nparts * num_heads;
+    w.lse_off = round_up(rows * head_dim * sizeof(float), 256);
+    w.cnt_off = w.lse_off + round_up(rows * sizeof(float), 256);
+    w.sched_off = w.cnt_off + round_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+  }
+  w.total = w.sched_off + kSchedBytes;
   return w;
 }
 
@@ -132,7 +137,7 @@ int32_t cascade_splits(int32_t num_groups, int32_t max_group_size, int32_t max_p
 // attention workspace).
 struct CascadeLayout {
   int32_t splits;
-  size_t lse_off, cu_off, ws_off, ws_bytes, total;
+  size_t lse_off, cu_off, ws_off, ws_bytes, ws_sched_off, total;
 };
 
 CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_group_size,
@@ -146,12 +151,25 @@ CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_g
   c.ws_off = c.cu_off + round_up((size_t)(num_seqs + 1) * sizeof(int32_t), 256);
   int32_t ps = 0, np = 1;
   resolve_partition(max_tail_len, -1, &ps, &np);
-  c.ws_bytes = workspace_layout(num_seqs, num_heads, head_dim, np).total;
+  const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, np);
+  c.ws_bytes = wl.total;
+  c.ws_sched_off = wl.sched_off;
   c.total = c.ws_off + c.ws_bytes;
   return c;
 }
 
 }  // namespace
+
+namespace pkv {
+size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size) {
+  int32_t ps = 0, np = 1;
+  if (num_seqs <= 0 || num_heads <= 0 || !resolve_partition(max_seq_len, partition_size, &ps, &np))
+    return 0;
+  const WorkspaceLayout w = workspace_layout(num_seqs, num_heads, 1, np);
+  return w.total - (np > 1 ? w.cnt_off : w.sched_off);
+}
+}  // namespace pkv
 
 extern "C" {
 
@@ -236,8 +254,8 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
   const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, np);
   const size_t need = wl.total;
-  if (need > 0 && (!workspace || workspace_bytes < need ||
-                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+  if (!workspace || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;
 
   AttnParams p;
@@ -264,6 +282,7 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.ws_out = nullptr;
   p.ws_lse = nullptr;
   p.ws_cnt = nullptr;
+  p.sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.sched_off);
   // the decode kernel takes requests of up to 32 (query, head) rows: two
   // subgroups of its 16-row MMA tiles
   p.decode_max_q = 32 / group > 1 ? 32 / group : 1;
@@ -272,7 +291,7 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.kv_splits = 1;
   p.split_out_stride = 0;
   p.split_lse_stride = 0;
-  if (need > 0) {
+  if (np > 1) {
     p.ws_out = static_cast<float*>(workspace);
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_off);
     p.ws_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.cnt_off);
@@ -377,7 +396,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
       part_out + (int64_t)c.splits * bh * head_dim, part_lse + (int64_t)c.splits * bh, q, kv_pool,
       tail_tables, max_tail_blocks, tail_cu, tail_lens, num_seqs, num_seqs, 1, max_tail_len,
       num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, -1,
-      c.ws_bytes > 0 ? ws + c.ws_off : nullptr, c.ws_bytes, dev_status, stream);
+      ws + c.ws_off, c.ws_bytes, dev_status, stream);
   if (s != PKV_OK) return s;
   // 3. prefixes: every group's queries against its shared blocks, once, on
   //    the tensor cores (the prefill kernel in prefix mode), cut into key
@@ -407,6 +426,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.ws_out = nullptr;
     p.ws_lse = nullptr;
     p.ws_cnt = nullptr;
+    p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
     p.status = dev_status;
     p.decode_max_q = 0;  // the prefix pass takes every group
     p.decode_max_rows = 0;

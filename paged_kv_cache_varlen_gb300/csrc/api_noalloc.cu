@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "../../include/pkv.h"
+#include "launch.h"
 
 namespace {
 
@@ -49,8 +50,6 @@ cudaError_t noalloc_scratch(void** out) {
   return cudaSuccess;
 }
 
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
 }  // namespace
 
 extern "C" pkv_status pkv_paged_attention_varlen_noalloc(
@@ -66,10 +65,11 @@ extern "C" pkv_status pkv_paged_attention_varlen_noalloc(
   void* scratch = nullptr;
   if (need > 0) {
     if (noalloc_scratch(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
-    // The split-KV merge counters (the last piece of the scratch) must start
-    // at zero. Calls leave them zero, but an interrupted call may not, so
-    // clear them every time.
-    const size_t cnt_bytes = round_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+    // The split-KV merge counters and the prefill work tickets (the last
+    // piece of the scratch) must start at zero. Calls leave them zero, but an
+    // interrupted call may not, so clear them every time.
+    const size_t cnt_bytes =
+        pkv::attention_zeroed_tail_bytes(num_seqs, num_heads, max_seq_len, partition_size);
     if (cudaMemsetAsync(static_cast<char*>(scratch) + (need - cnt_bytes), 0, cnt_bytes,
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return PKV_ERR_CUDA;

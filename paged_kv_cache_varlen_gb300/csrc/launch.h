@@ -38,6 +38,8 @@ struct AttnParams {
   float* ws_out;              // [B][num_parts][H][D] (null when num_parts == 1)
   float* ws_lse;              // [B][num_parts][H]
   int32_t* ws_cnt;            // [B][H] arrival counters, zero between calls
+  int32_t* sched;             // prefill work tickets: [0] next item, [1] CTAs done;
+                              // zero between calls
   int32_t* status;
   // shared-prefix (cascade) pass of the prefill kernel: every query of a
   // "request" (a prefix group) sees all seq_len keys, no causal mask; the
@@ -54,6 +56,12 @@ struct AttnParams {
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
+
+// Bytes at the end of an attention workspace that must be zero before a call
+// (and that every completed call leaves zero): the split-KV arrival counters
+// and the prefill work tickets.
+size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size);
 
 // Decode kernel (query_len == 1 requests): TMA-staged pages, QK^T and PV on
 // the warp-level tensor cores (mma.sync), split-KV partitions merged

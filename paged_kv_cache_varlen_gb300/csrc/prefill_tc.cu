@@ -13,10 +13,11 @@
 //
 // GB300 design:
 //   * persistent CTAs, one per SM: every CTA builds the per-request prefix
-//     sum of work items in shared memory and takes items blockIdx.x,
-//     blockIdx.x + gridDim.x, ...; an item is (request, KV head, two
-//     consecutive query tiles A and B of 128/G queries each), later items
-//     (more keys) first. Tensor memory and barriers are set up once per CTA,
+//     sum of work items in shared memory and takes items dynamically from a
+//     global ticket counter in the workspace (the busiest SM had 1.6x the
+//     mean work under a static round-robin); an item is (request, KV head,
+//     two consecutive query tiles A and B of 128/G queries each), later
+//     items (more keys) first. Tensor memory and barriers are set up once per CTA,
 //     and no CTA is launched for decode requests;
 //   * a Q tile is 128 rows = (128/G queries) x (G heads sharing the KV head),
 //     so one pass over the K/V pages serves the whole GQA group, and both Q
@@ -72,6 +73,10 @@ constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // first producer warp (als
 constexpr int kMmaWarp = kProdWarp0 + kProducers / 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kRing = 4;  // work items announced ahead of the roles that consume them
+// readers of an announced item: the second producer warp, the MMA thread and
+// the eight softmax warps (one lane each)
+constexpr int kItemReaders = 1 + 1 + kSoftmaxThreads / 32;
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
 
@@ -110,6 +115,8 @@ struct Bars {
   uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
   uint64_t o_free[kQT];   // the warpgroup's epilogue has read O_x
   uint64_t mma_done;
+  uint64_t item_full[kRing], item_empty[kRing];
+  int32_t item_id[kRing];  // work item taken from the global ticket counter, -1: none left
   uint32_t tmem_base;
   int32_t abort;
   int32_t scan[kThreads / 32];
@@ -231,6 +238,46 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
   return d;
 }
 
+// Work items are handed out dynamically: the first producer warp takes the
+// next ticket from the global counter p.sched[0] and announces it in a small
+// ring; every other role reads the same sequence from the ring. A CTA that
+// finishes counts itself in p.sched[1]; the last one resets both counters, so
+// they are zero again for the next call.
+__device__ __forceinline__ int take_item(Bars* bars, const AttnParams& p, int total, int k,
+                                         volatile int32_t* abort) {
+  const int slot = k % kRing;
+  bool w = true;
+  if (k >= kRing)
+    w = mbar_wait(smem_addr(&bars->item_empty[slot]), ((k / kRing) - 1) & 1, p.status, abort);
+  int it = -1;
+  if (w) {
+    const int t = atomicAdd(p.sched, 1);
+    it = t < total ? t : -1;
+  }
+  *reinterpret_cast<volatile int32_t*>(&bars->item_id[slot]) = it;
+  mbar_arrive(smem_addr(&bars->item_full[slot]));
+  return it;
+}
+
+__device__ __forceinline__ int read_item(Bars* bars, const AttnParams& p, int k,
+                                         volatile int32_t* abort) {
+  const int slot = k % kRing;
+  int it = -1;
+  if (mbar_wait(smem_addr(&bars->item_full[slot]), (k / kRing) & 1, p.status, abort))
+    it = *reinterpret_cast<volatile int32_t*>(&bars->item_id[slot]);
+  mbar_arrive(smem_addr(&bars->item_empty[slot]));
+  return it;
+}
+
+__device__ __forceinline__ void cta_finished(const AttnParams& p) {  // one thread
+  __threadfence();
+  if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+    p.sched[0] = 0;
+    p.sched[1] = 0;
+    __threadfence();
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map, const AttnParams p) {
@@ -268,11 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bars->o_free[x]), kBM);
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
+    for (int k = 0; k < kRing; ++k) {
+      mbar_init(smem_addr(&bars->item_full[k]), 1);
+      mbar_init(smem_addr(&bars->item_empty[k]), kItemReaders);
+    }
     bars->abort = 0;
     fence_barrier_init();
   }
   const int total = prefill_prefix(p, pref, bars->scan, QP) * p.num_kv_heads;  // syncs
-  if ((int)blockIdx.x >= total) return;  // uniform; nothing allocated yet
+  if ((int)blockIdx.x >= total) {  // uniform; nothing allocated yet
+    if (threadIdx.x == 0) cta_finished(p);
+    return;
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -310,7 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (qlead) prefetch_tmap(&q_map);
     int gi = 0, gt = 0, armed = 0, q_issued = 0;
     bool ok = true, bad_block = false;
-    for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
+    for (;; ++gi) {
+      int it = -1;
+      if (lane == 0)
+        it = warp == kProdWarp0 ? take_item(bars, p, total, gi, abort)
+                                : read_item(bars, p, gi, abort);
+      it = __shfl_sync(kFullMask, it, 0);
+      if (it < 0) break;
       const PrefillItem d = prefill_item(p, pref, QP, it);
       const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
       if (warp == kProdWarp0) {
@@ -444,7 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return mbar_wait(smem_addr(bar), parity, p.status, abort);
       };
-      for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++gi) {
+      for (; ok; ++gi) {
+        const int it = read_item(bars, p, gi, abort);
+        if (it < 0) break;
         const PrefillItem d = prefill_item(p, pref, QP, it);
         const int n = d.n_tiles;
         ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
@@ -494,7 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     int gt = 0;
-    for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (int k = 0; ok; ++k) {
+      int it = -1;
+      if (lane == 0) it = read_item(bars, p, k, abort);
+      it = __shfl_sync(kFullMask, it, 0);
+      if (it < 0) break;
       const PrefillItem d = prefill_item(p, pref, QP, it);
       const int qj = d.j0 + x * QT + rq;
       const bool row_valid = qj < d.j1;
@@ -665,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) cta_finished(p);
 }
 
 template <int D>
