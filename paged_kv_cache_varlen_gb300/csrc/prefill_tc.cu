@@ -17,8 +17,9 @@
 //     global ticket counter in the workspace (the busiest SM had 1.6x the
 //     mean work under a static round-robin); an item is (request, KV head,
 //     two consecutive query tiles A and B of 128/G queries each), later
-//     items (more keys) first. Tensor memory and barriers are set up once per CTA,
-//     and no CTA is launched for decode requests;
+//     items (more keys) first. Tensor memory and barriers are set up once per CTA;
+//     requests short enough for the decode kernel (1 .. decode_max_q
+//     queries) give no items here;
 //   * a Q tile is 128 rows = (128/G queries) x (G heads sharing the KV head),
 //     so one pass over the K/V pages serves the whole GQA group, and both Q
 //     tiles of the item share every K/V tile loaded: the gather from L2 (the
@@ -140,7 +141,8 @@ __device__ __forceinline__ int prefix_segment_count(int L, int splits) {
   return tps > 0 ? (t + tps - 1) / tps : 0;
 }
 
-// Work units (pairs of query tiles) of request r (0 for decode requests);
+// Work units (pairs of query tiles) of request r (0 for requests of at most
+// decode_max_q queries, which the decode kernel takes);
 // bad lengths flagged by CTA 0. QP = queries per unit.
 __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP, bool flag) {
   const int32_t t0 = __ldg(p.cu_seqlens + r), t1 = __ldg(p.cu_seqlens + r + 1);
