@@ -90,8 +90,8 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
  * (at least 256: the prefill kernel's work tickets; split-KV partials on top;
  * 0 only for invalid sizes). The caller allocates it (a 256-byte aligned
  * device buffer at least this large) and ZERO-FILLS it once before its first
- * use (it holds per-request arrival counters of the split-KV merge and the
- * counter from which prefill CTAs take their work items). Every call that
+ * use (it holds the counter from which prefill CTAs take their work items;
+ * the split-KV partials need no clearing). Every call that
  * completes without PKV_DEV_TIMEOUT leaves it zero-filled again, so one
  * workspace serves any number of calls on one stream; calls that may run
  * concurrently need separate workspaces. After a PKV_DEV_TIMEOUT, clear it
@@ -199,8 +199,8 @@ pkv_status pkv_lse_merge(float *out, float *out_lse, const float *part_out,
  *   the device.
  * - Every call on a device shares the one array, which keeps the last call's
  *   contents: calls that may overlap on the GPU (other streams, other host
- *   threads) race on it. The merge counters inside it are cleared by every
- *   call.
+ *   threads) race on it. The work-ticket counter inside it is cleared by
+ *   every call.
  */
 pkv_status pkv_paged_attention_varlen_noalloc(
     float *out, float *out_lse, const void *q, const void *kv_pool, const int32_t *block_table,

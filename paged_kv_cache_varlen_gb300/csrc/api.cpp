@@ -79,7 +79,7 @@ bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps,
   int32_t s = partition_size == 0 ? ((len + 15) / 16) * 16
                                   : (partition_size < 0 ? kAutoPartition : partition_size);
   // automatic: kAutoPartition tokens, doubled until at most kMaxAutoParts per
-  // request (also bounds the partials the in-kernel merge reads)
+  // request (also bounds the partials the merge reads)
   while (partition_size < 0 && (len + s - 1) / s > kMaxAutoParts) s *= 2;
   int32_t n = (len + s - 1) / s;
   if (n <= 1) {
@@ -99,17 +99,16 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kSchedBytes = 256;
 
 struct WorkspaceLayout {
-  size_t lse_off, cnt_off, sched_off, total;
+  size_t lse_off, sched_off, total;
 };
 
 WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                                  int32_t nparts) {
-  WorkspaceLayout w{0, 0, 0, 0};
+  WorkspaceLayout w{0, 0, 0};
   if (nparts > 1) {
     const size_t rows = (size_t)num_seqs * nparts * num_heads;
     w.lse_off = round_up(rows * head_dim * sizeof(float), 256);
-    w.cnt_off = w.lse_off + round_up(rows * sizeof(float), 256);
-    w.sched_off = w.cnt_off + round_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+    w.sched_off = w.lse_off + round_up(rows * sizeof(float), 256);
   }
   w.total = w.sched_off + kSchedBytes;
   return w;
@@ -167,7 +166,7 @@ size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t 
   if (num_seqs <= 0 || num_heads <= 0 || !resolve_partition(max_seq_len, partition_size, &ps, &np))
     return 0;
   const WorkspaceLayout w = workspace_layout(num_seqs, num_heads, 1, np);
-  return w.total - (np > 1 ? w.cnt_off : w.sched_off);
+  return w.total - w.sched_off;
 }
 }  // namespace pkv
 
@@ -281,7 +280,6 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   p.num_parts = np;
   p.ws_out = nullptr;
   p.ws_lse = nullptr;
-  p.ws_cnt = nullptr;
   p.sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.sched_off);
   // the decode kernel takes requests of up to 32 (query, head) rows: two
   // subgroups of its 16-row MMA tiles
@@ -294,7 +292,6 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   if (np > 1) {
     p.ws_out = static_cast<float*>(workspace);
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_off);
-    p.ws_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.cnt_off);
   }
   p.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -425,8 +422,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.num_parts = 1;
     p.ws_out = nullptr;
     p.ws_lse = nullptr;
-    p.ws_cnt = nullptr;
-    p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
+      p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
     p.status = dev_status;
     p.decode_max_q = 0;  // the prefix pass takes every group
     p.decode_max_rows = 0;

@@ -65,8 +65,8 @@ extern "C" pkv_status pkv_paged_attention_varlen_noalloc(
   void* scratch = nullptr;
   if (need > 0) {
     if (noalloc_scratch(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
-    // The split-KV merge counters and the prefill work tickets (the last
-    // piece of the scratch) must start at zero. Calls leave them zero, but an
+    // The prefill work tickets (the last piece of the scratch) must start
+    // at zero. Calls leave them zero, but an
     // interrupted call may not, so clear them every time.
     const size_t cnt_bytes =
         pkv::attention_zeroed_tail_bytes(num_seqs, num_heads, max_seq_len, partition_size);

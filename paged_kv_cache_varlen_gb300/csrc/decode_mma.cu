@@ -36,8 +36,12 @@
 //     with V rows from ldmatrix.trans; V rows of tokens past the context are
 //     zeroed first (P is 0 there, and 0 * NaN is not);
 //   * end: warps merge through shared memory; a split request's partitions
-//     are merged by the last partition CTA to finish, as in the CUDA-core
-//     kernel; programmatic dependent launch as well.
+//     write normalised partials and leave at once, and a small merge grid,
+//     launched behind it with programmatic dependent launch, combines them
+//     (per-CTA timelines showed the CTA that merged in-kernel spending ~8 us
+//     of dependent memory round trips at the end of the grid);
+//   * the prologue reads the request's lengths and the first block ids in
+//     one round trip, so the first copies leave ~1 round trip earlier.
 #include <math.h>
 
 #include "common.cuh"
@@ -97,7 +101,6 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* slots = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * SPW * SLOT);
-  int* flag = reinterpret_cast<int*>(bars + kWarps * SPW);
 
   // Everything below may read the pool the preceding KV write produces.
   griddep_wait();
@@ -116,8 +119,24 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int i = blockIdx.z;
   const bool leader = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
-  const int32_t t0 = p.cu_seqlens[i];
-  const int32_t t1 = p.cu_seqlens[i + 1];
+  // The request's lengths and the block ids of this warp's first chunks are
+  // fetched together, one memory round trip before the first copy is issued
+  // (the ids are read speculatively, bounded by the table row only).
+  const int32_t t0 = __ldg(p.cu_seqlens + i);
+  const int32_t t1 = __ldg(p.cu_seqlens + i + 1);
+  const int32_t L = __ldg(p.seq_lens + i);
+  // several queries (a verification step) take partition 0 only, kbeg = 0
+  const int32_t kbeg = part * p.part_size;
+  const int32_t* bt = p.block_table + (int64_t)i * p.max_blocks;
+  // lane j of the warp caches the block id of the warp's chunk (kb + j)
+  auto load_ids = [&](int kb) -> int32_t {
+    const int64_t c = warp + (int64_t)(kb + lane) * kWarps;
+    const int64_t blk = (kbeg + c * kChunk) / p.block_size;
+    return blk < p.max_blocks ? __ldg(bt + blk) : -1;
+  };
+  int32_t ids_cur = load_ids(0);
+  int32_t ids_next = load_ids(32);
+
   if (t0 < 0 || t1 < t0 || t1 > p.num_tokens) {
     if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return;
@@ -127,15 +146,13 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int row0 = sub * kRows;
   if (row0 >= qlen * group) return;  // no row of this request in the subgroup
   const int rows = min(kRows, qlen * group - row0);  // rows of this CTA
-  const int32_t L = p.seq_lens[i];
   if (L < qlen || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
     if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return;
   }
-  // several queries (a verification step): one partition over every key,
-  // with the causal limit per row; one query: the split-KV partitions
+  // several queries: one partition over every key, with the causal limit per
+  // row; one query: the split-KV partitions
   if (qlen > 1 && part > 0) return;
-  const int32_t kbeg = qlen > 1 ? 0 : part * p.part_size;
   if (kbeg >= L) return;
   const int32_t kend = qlen > 1 ? L : min(L, kbeg + p.part_size);
   const int nchunks = (kend - kbeg + kChunk - 1) / kChunk;
@@ -148,14 +165,6 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   if (warp == 0 && lane == 0) prefetch_tmap(&kv_map);
   __syncwarp();
 
-  const int32_t* bt = p.block_table + (int64_t)i * p.max_blocks;
-  // lane j of the warp caches the block id of the warp's chunk (kb + j)
-  auto load_ids = [&](int kb) -> int32_t {
-    const int k = kb + lane;
-    if (k >= my_chunks) return -1;
-    const int c = warp + k * kWarps;
-    return __ldg(bt + (kbeg + c * kChunk) / p.block_size);
-  };
   const int32_t nrows = p.num_blocks * p.block_size;
   auto issue = [&](int k, int32_t id) {  // lane 0 only
     const int slot = k % SPW;
@@ -173,8 +182,6 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     tma_load_4d(dst + HALF, &kv_map, bar, 0, 0, kvh, row + nrows);
   };
 
-  int32_t ids_cur = load_ids(0);
-  int32_t ids_next = load_ids(32);
   int issued = 0;
   for (int k = 0; k < SPW && k < my_chunks; ++k) {
     const int32_t id = __shfl_sync(kFull, ids_cur, k);
@@ -402,59 +409,110 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       if (d == 0) p.ws_lse[rr] = lse;
     }
   }
-  if (parts_i == 1) return;
+}
 
-  // ---- split request (one query): the last partition CTA of (request, head
-  // subgroup) merges; counters [request][KV head][subgroup of the heads]
-  const int nsub1 = (group + kRows - 1) / kRows;
-  int32_t* cnt = p.ws_cnt + ((int64_t)i * p.num_kv_heads + kvh) * nsub1 + sub;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();  // publish this CTA's partial before counting it
-    const int old = atomicAdd(cnt, 1);
-    *flag = (old == parts_i - 1);
-  }
-  __syncthreads();
-  if (!*flag) return;
-  __threadfence();  // see every other partition's partial
-  float* mg = red_ml;  // [rows] maxima of the partial lse (reuses shared memory)
-  const int64_t wrow0 = (int64_t)i * p.num_parts * p.num_heads;
-  for (int g = warp; g < rows; g += kWarps) {
-    float M = -INFINITY;
-    for (int pp = lane; pp < parts_i; pp += 32)
-      M = fmaxf(M, __ldcg(p.ws_lse + wrow0 + (int64_t)pp * p.num_heads + h0 + g));
+// Split requests (one query, two or more partitions): the partitions'
+// normalised outputs combined by their log-sum-exp (page 1 §07), as a
+// separate grid so that no attention CTA waits on the others. WPR warps per
+// (request, head) row split the partitions (one row per CTA when WPR > 1,
+// four when WPR == 1); lanes hold float4 slices of D. Each warp makes one
+// pass with a running maximum, so its partitions' loads can all be in
+// flight; the warps then combine through shared memory.
+template <int D, int WPR>
+__global__ void __launch_bounds__(128 * (WPR == 1 ? 1 : WPR / 4))
+    decode_merge_kernel(const AttnParams p) {
+  constexpr int R = WPR == 1 ? 4 : 1;  // rows per CTA
+  constexpr int RS = D + 4;  // floats per warp record: D, max, sum (16-byte multiple)
+  __shared__ __align__(16) float red[WPR > 1 ? WPR * RS : 4];
+  griddep_wait();  // the attention grid and its partials are complete
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int h = blockIdx.x * R + (R > 1 ? warp : 0);
+  const int wr = R > 1 ? 0 : warp;  // this warp's share of the row's partitions
+  const int i = blockIdx.y;
+  if (h >= p.num_heads) return;  // (uniform over the CTA when WPR > 1)
+  const int32_t t0 = __ldg(p.cu_seqlens + i);
+  const int32_t t1 = __ldg(p.cu_seqlens + i + 1);
+  const int32_t L = __ldg(p.seq_lens + i);
+  // requests the attention kernel rejected (and flagged) or did not split
+  if (t0 < 0 || t1 != t0 + 1 || t1 > p.num_tokens) return;
+  if (L < 1 || L > p.max_seq_len || L > p.max_blocks * p.block_size) return;
+  const int parts = (L + p.part_size - 1) / p.part_size;
+  if (parts < 2) return;
+  const int64_t r0 = (int64_t)i * p.num_parts * p.num_heads + h;
+  const bool act = lane < D / 4;
+  float M = -INFINITY, wsum = 0.f;  // log2 domain
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int U = 8;  // partitions in flight per warp
+  for (int base = wr; base < parts; base += U * WPR) {
+    float l[U];
+    float4 ov[U];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    if (lane == 0) mg[g] = M;
+    for (int u = 0; u < U; ++u) {
+      const int pp = base + u * WPR;
+      const int64_t rr = r0 + (int64_t)pp * p.num_heads;
+      l[u] = pp < parts ? __ldcg(p.ws_lse + rr) * kLog2e : -INFINITY;
+      ov[u] = (pp < parts && act)
+                  ? __ldcg(reinterpret_cast<const float4*>(p.ws_out + rr * D) + lane)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (l[u] == -INFINITY) continue;  // past the last partition
+      if (l[u] > M) {
+        const float c = fast_exp2(M - l[u]);  // 0 while M is -inf
+        wsum *= c;
+        acc.x *= c;
+        acc.y *= c;
+        acc.z *= c;
+        acc.w *= c;
+        M = l[u];
+      }
+      const float w = fast_exp2(l[u] - M);
+      wsum += w;
+      acc.x += w * ov[u].x;
+      acc.y += w * ov[u].y;
+      acc.z += w * ov[u].z;
+      acc.w += w * ov[u].w;
+    }
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < rows * D / 4; idx += kWarps * 32) {
-    const int g = idx / (D / 4);
-    const int d4 = idx - g * (D / 4);
-    const float M = mg[g];
-    const int h = h0 + g;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll 4
-      for (int pp = 0; pp < parts_i; ++pp) {
-        const int64_t rr = wrow0 + (int64_t)pp * p.num_heads + h;
-        const float w = fast_exp2((__ldcg(p.ws_lse + rr) - M) * kLog2e);  // 0 for an empty part
-        const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.ws_out + rr * D) + d4);
-        wsum += w;
-        acc.x += w * ov.x;
-        acc.y += w * ov.y;
-        acc.z += w * ov.z;
-        acc.w += w * ov.w;
+  if (WPR > 1) {
+    float* mine = red + warp * RS;
+    if (act) reinterpret_cast<float4*>(mine)[lane] = acc;
+    if (lane == 0) {
+      mine[D] = M;
+      mine[D + 1] = wsum;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) Mt = fmaxf(Mt, red[w * RS + D]);
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    wsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) {
+      const float mw = red[w * RS + D];
+      if (mw == -INFINITY) continue;
+      const float c = fast_exp2(mw - Mt);
+      wsum += c * red[w * RS + D + 1];
+      if (act) {
+        const float4 x = reinterpret_cast<const float4*>(red + w * RS)[lane];
+        acc.x += c * x.x;
+        acc.y += c * x.y;
+        acc.z += c * x.z;
+        acc.w += c * x.w;
       }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    reinterpret_cast<float4*>(p.out + ((int64_t)t0 * p.num_heads + h) * D)[d4] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (d4 == 0 && p.out_lse)
-      p.out_lse[(int64_t)t0 * p.num_heads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+    M = Mt;
   }
-  if (threadIdx.x == 0) *cnt = 0;  // ready for reuse
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t orow = (int64_t)t0 * p.num_heads + h;
+  if (act)
+    reinterpret_cast<float4*>(p.out + orow * D)[lane] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (lane == 0 && p.out_lse) p.out_lse[orow] = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
 }
 
 #ifndef PKV_DECODE_MMA_MINB
@@ -489,7 +547,19 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, kv_map, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, kv_map, p);
+  if (e != cudaSuccess || p.num_parts < 2) return e;
+  // few partitions: a warp per row; many: eight warps split a row's
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.dynamicSmemBytes = 0;
+  if (p.num_parts <= 8) {
+    mcfg.gridDim = dim3((p.num_heads + 3) / 4, p.num_seqs);
+    mcfg.blockDim = dim3(128);
+    return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<D, 1>, p);
+  }
+  mcfg.gridDim = dim3(p.num_heads, p.num_seqs);
+  mcfg.blockDim = dim3(256);
+  return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<D, 8>, p);
 }
 
 }  // namespace

@@ -37,7 +37,6 @@ struct AttnParams {
   int32_t num_parts;          // partitions per request covering max_seq_len
   float* ws_out;              // [B][num_parts][H][D] (null when num_parts == 1)
   float* ws_lse;              // [B][num_parts][H]
-  int32_t* ws_cnt;            // [B][H] arrival counters, zero between calls
   int32_t* sched;             // prefill work tickets: [0] next item, [1] CTAs done;
                               // zero between calls
   int32_t* status;
@@ -58,14 +57,13 @@ struct AttnParams {
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 
 // Bytes at the end of an attention workspace that must be zero before a call
-// (and that every completed call leaves zero): the split-KV arrival counters
-// and the prefill work tickets.
+// (and that every completed call leaves zero): the prefill work tickets.
 size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size);
 
 // Decode kernel (query_len == 1 requests): TMA-staged pages, QK^T and PV on
-// the warp-level tensor cores (mma.sync), split-KV partitions merged
-// in-kernel by the last partition CTA. `kv_map` views the pool as
+// the warp-level tensor cores (mma.sync); split-KV partitions merged by a
+// second, small grid launched behind it. `kv_map` views the pool as
 // [2*NB*BS rows][Hkv][D/64][64] with a box of {64, D/64, 1, 16} and 128-byte
 // swizzle. Up to 16 query heads per CTA.
 cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,

@@ -51,9 +51,9 @@ def test_workspace_size_arithmetic(lib):
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 512, -1) == sched
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 0) == sched
     # 4096 / 1024 = 4 partitions: [B][4][H][D] fp32 partials + [B][4][H] fp32 lse
-    # + [B][H] int32 merge counters + tickets, each piece 256-byte aligned
+    # + tickets, each piece 256-byte aligned
     rows = 64 * 4 * 32
-    expect = up(rows * 128 * 4) + up(rows * 4) + up(64 * 32 * 4) + sched
+    expect = up(rows * 128 * 4) + up(rows * 4) + sched
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, -1) == expect
     assert lib.pkv_attention_workspace_size(64, 64, 32, 8, 128, 4096, 1024) == expect
     # explicit partition must be a multiple of 16
@@ -61,7 +61,7 @@ def test_workspace_size_arithmetic(lib):
     # automatic partitions double until a request has at most 32 of them
     rows = 8 * 32 * 32            # 131072 tokens -> 4096-token partitions -> 32 parts
     assert lib.pkv_attention_workspace_size(8, 8, 32, 8, 128, 131072, -1) == \
-        up(rows * 128 * 4) + up(rows * 4) + up(8 * 32 * 4) + sched
+        up(rows * 128 * 4) + up(rows * 4) + sched
 
 
 def _attn(lib, **over):
