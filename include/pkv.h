@@ -87,8 +87,9 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
 /*
  * pkv_attention_workspace_size -- bytes of scratch that
  * pkv_paged_attention_varlen needs for these sizes and this partition_size
- * (at least 256: the prefill kernel's work tickets; split-KV partials on top;
- * 0 only for invalid sizes). The caller allocates it (a 256-byte aligned
+ * (at least 256: the prefill kernel's work tickets; split-KV partials on top:
+ * [num_seqs][P][H][D] + [num_seqs][P][H] fp32 for P partitions; 0 only for
+ * invalid sizes). The caller allocates it (a 256-byte aligned
  * device buffer at least this large) and ZERO-FILLS it once before its first
  * use (it holds the counter from which prefill CTAs take their work items;
  * the split-KV partials need no clearing). Every call that
@@ -129,7 +130,8 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  *                requests: 0 = never split; -1 = automatic (1024 tokens,
  *                doubled until no request has more than 32 partitions);
  *                > 0 = that many tokens, a multiple of 16. A split request's
- *                partitions are merged by log-sum-exp inside the same kernel
+ *                partitions are merged by log-sum-exp in a small second grid
+ *                behind the first
  *   workspace, workspace_bytes: scratch of at least
  *                pkv_attention_workspace_size(...) bytes, zero-filled before
  *                its first use (see there)
@@ -138,9 +140,12 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  * and attends to keys 0..pos (bottom-right causal alignment). Keys beyond
  * seq_len_i are never read, so unwritten slots of a partial last block may
  * hold anything, NaN included.
- * Requests with query_len == 1 run on the decode kernel (CUDA cores,
- * HBM-bound, split-KV + log-sum-exp merge when partitioned); requests with
- * query_len > 1 run on the chunked-prefill kernel (tcgen05 tensor cores).
+ * Requests of 1 .. max(1, 32 / G) queries (decode, and speculative
+ * verification steps; G = num_heads / num_kv_heads) run on the decode kernel
+ * (HBM-bound, warp-level tensor-core products; query_len == 1 requests split
+ * into partitions merged by log-sum-exp, several-query requests one
+ * partition); longer requests run on the chunked-prefill kernel (tcgen05
+ * tensor cores).
  * The kernels use programmatic dependent launch: each waits for the grid
  * before it in the stream to finish before touching memory, so ordinary
  * stream order holds.
