@@ -77,6 +77,36 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
+def split_parts(max_seq_len: int, partition_size: int) -> int:
+    """Split-KV partitions per request, as the library resolves them: 1024
+    tokens doubled until at most 32 (automatic), none (0) or the given size."""
+    length = max(int(max_seq_len), 1)
+    if partition_size == 0:
+        return 1
+    s = 1024 if partition_size < 0 else partition_size
+    while partition_size < 0 and -(-length // s) > 32:
+        s *= 2
+    return max(1, -(-length // s))
+
+
+def attention_launches(w, partition_size: int, ci) -> int:
+    """Kernels one attention call launches: the decode grid, the split-KV
+    merge grid when requests split, the prefill grid when a request has more
+    queries than the decode kernel takes; the cascade call adds its prepare
+    kernel, the prefix pass and the final merge around the tail decode."""
+    if ci is not None:
+        tail = 1 + (1 if split_parts(ci["max_tail_len"], -1) > 1 else 0)
+        return 1 + tail + (1 if len(ci["prefix_lens"]) else 0) + 1
+    group = w.num_heads // w.num_kv_heads
+    dmq = max(1, 32 // group)
+    n = 1
+    if split_parts(w.max_seq_len, partition_size) > 1:
+        n += 1
+    if w.max_query_len > dmq:
+        n += 1
+    return n
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("decode_mma.cu", "merge.cu", "common.cuh"):
@@ -421,8 +451,7 @@ def run_ours(args):
     # may legitimately be served from L2, or be read once per group)
     roof_bytes = w.unique_kv_bytes() if "prefix_tokens" in w.meta else kv_bytes
     achieved = roof_bytes / (attn_avg_ms * 1e-3) / 1e9
-    # write, decode, [prefill]; cascade: write, prepare, decode, prefix pass, merge
-    launches_per_step = 5 if ci is not None else 2 + (1 if w.max_query_len > 1 else 0)
+    launches_per_step = 1 + attention_launches(w, args.partition_size, ci)
     prefill_line = None
     flops = w.attention_flops(2)
     if flops > 0:

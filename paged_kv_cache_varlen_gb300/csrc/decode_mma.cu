@@ -424,17 +424,21 @@ __global__ void __launch_bounds__(128 * (WPR == 1 ? 1 : WPR / 4))
   constexpr int R = WPR == 1 ? 4 : 1;  // rows per CTA
   constexpr int RS = D + 4;  // floats per warp record: D, max, sum (16-byte multiple)
   __shared__ __align__(16) float red[WPR > 1 ? WPR * RS : 4];
-  griddep_wait();  // the attention grid and its partials are complete
-  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int h = blockIdx.x * R + (R > 1 ? warp : 0);
   const int wr = R > 1 ? 0 : warp;  // this warp's share of the row's partitions
   const int i = blockIdx.y;
+  // The lengths are inputs that the attention grid does not write. This grid
+  // starts only once every attention CTA has passed its own wait on the
+  // grids before it, so they are final; they are read (through L2) while the
+  // attention grid is still running, off the path after its completion.
+  const int32_t t0 = __ldcg(p.cu_seqlens + i);
+  const int32_t t1 = __ldcg(p.cu_seqlens + i + 1);
+  const int32_t L = __ldcg(p.seq_lens + i);
+  griddep_wait();  // the attention grid and its partials are complete
+  griddep_launch_dependents();
   if (h >= p.num_heads) return;  // (uniform over the CTA when WPR > 1)
-  const int32_t t0 = __ldg(p.cu_seqlens + i);
-  const int32_t t1 = __ldg(p.cu_seqlens + i + 1);
-  const int32_t L = __ldg(p.seq_lens + i);
   // requests the attention kernel rejected (and flagged) or did not split
   if (t0 < 0 || t1 != t0 + 1 || t1 > p.num_tokens) return;
   if (L < 1 || L > p.max_seq_len || L > p.max_blocks * p.block_size) return;

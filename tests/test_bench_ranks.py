@@ -95,3 +95,21 @@ def test_reference_arm_rank1_does_no_work(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
     assert bench.main() == 0
     assert capsys.readouterr().out == ""
+
+
+def test_split_parts_follows_the_library():
+    """bench.py counts the merge grid from its own copy of the partition
+    rule; the library's workspace size (partials for every partition) pins
+    that copy: partials exist exactly when the count is above 1, and their
+    size is the count's."""
+    from paged_kv_cache_varlen_gb300 import binding
+    lib = binding.load_library()
+    B, H, D = 8, 32, 128
+    up = lambda x: -(-x // 256) * 256
+    for L in (1, 16, 1000, 1024, 1025, 4096, 4097, 32768, 32769, 131072, 200000):
+        for ps in (-1, 0, 16, 512, 2048):
+            n = bench.split_parts(L, ps)
+            ws = lib.pkv_attention_workspace_size(B, B, H, 8, D, L, ps)
+            rows = B * n * H
+            want = 256 if n == 1 else up(rows * D * 4) + up(rows * 4) + 256
+            assert ws == want, (L, ps, n, ws, want)
