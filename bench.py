@@ -232,12 +232,15 @@ def oracle_step(orc, w):
     orc.paged_attention(w.q, pool, w.block_table, w.cu_seqlens, w.seq_lens, w.scale)
 
 
-def oracle_step_seconds(w, budget_s: float):
+def oracle_step_seconds(w, budget_s: float, threads: int = 0):
     """Time the oracle on whole steps of the workload; repeat until about
-    `budget_s` seconds of CPU time. Returns the median step time."""
+    `budget_s` seconds of CPU time. Returns the median step time, the
+    threads used (all cores of the affinity mask unless `threads` is given)
+    and the number of steps."""
     import oracle as oracle_pkg
 
     orc = oracle_pkg.load()
+    orc.set_num_threads(threads if threads > 0 else len(os.sched_getaffinity(0)))
     cores = orc.num_threads()
     times = []
     t_all = time.perf_counter()
@@ -459,17 +462,24 @@ def run_ours(args):
         # also holds the decode kernel when the batch has decodes
         tpeak, tkind = tensor_peak()
         tflops = flops / (attn_avg_ms * 1e-3) / 1e12
+        # serial bound of the whole call: every K/V byte at the HBM peak plus
+        # the prefill FLOPs at the tensor peak
+        t_star_us = 1e6 * (kv_bytes / (peak * 1e9) + flops / (tpeak * 1e12))
         prefill_line = {"flops_per_step": flops, "achieved_tflops": tflops, "peak_tflops": tpeak,
                         "peak_kind": tkind, "frac": tflops / tpeak,
+                        "t_star_us": t_star_us, "t_star_frac": t_star_us / (attn_avg_ms * 1e3),
                         "time": "attention call" + (" (decode kernel included)"
                                                     if (w.query_lens == 1).any() else "")}
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         sample, desc = oracle_sample(w)
         sec, cores, n = oracle_step_seconds(sample, args.cpu_seconds)
+        sec1, _, n1 = oracle_step_seconds(sample, args.cpu_seconds / 4, threads=1)
         cpu = {"value": sample.kv_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
                "kind": "oracle", "sample": f"{desc}; {n} oracle steps, median",
-               "seqs_per_s": sample.num_seqs / sec}
+               "seqs_per_s": sample.num_seqs / sec,
+               "single_core": {"value": sample.kv_bytes() / sec1 / 1e9, "unit": "GB/s",
+                               "steps": n1}}
     if rank == 0:
         line = {
             "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
@@ -477,6 +487,13 @@ def run_ours(args):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
+            # one attention layer per step; a 32-layer model's decode step
+            # would repeat it 32 times
+            "seqs_per_s_32_layers": world * w.num_seqs / (ms_per_step * 1e-3) / 32,
+            "attention_us": {"mean": attn_avg_ms * 1e3,
+                             "p10": 1e3 * float(np.percentile(attn_ms, 10)),
+                             "p50": 1e3 * float(np.percentile(attn_ms, 50)),
+                             "p90": 1e3 * float(np.percentile(attn_ms, 90))},
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "config": workload_config(w, args.partition_size, world),
             "roofline": {"bound": "hbm",
