@@ -174,8 +174,9 @@ pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
  *
  * Per row: M = max_p lse_p, w_p = exp(lse_p - M),
  *   out = sum_p w_p * part_out_p / sum_p w_p,  lse = M + ln(sum_p w_p).
- * A partition with lse = -inf is empty and its part_out is not read; a row
- * whose partitions are all empty gives out = 0 and lse = -inf.
+ * A partition with lse = -inf is empty: its part_out values never enter the
+ * sums (they may hold anything, NaN included); a row whose partitions are
+ * all empty gives out = 0 and lse = -inf.
  * head_dim must be a multiple of 4 (at most 512); pointers 16-byte aligned.
  */
 pkv_status pkv_lse_merge(float *out, float *out_lse, const float *part_out,

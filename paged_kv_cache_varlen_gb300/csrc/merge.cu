@@ -5,12 +5,13 @@
 // renormalise them with log-sum-exp. For a row with partials (o_p, lse_p):
 //   M = max_p lse_p, w_p = exp(lse_p - M),
 //   o = sum_p w_p o_p / sum_p w_p,  lse = M + ln sum_p w_p.
-// A partial with lse = -inf is empty: it is skipped and its o_p never read.
-// A row whose partials are all empty gives o = 0, lse = -inf.
+// A partial with lse = -inf is empty: its o_p never enters a sum (it may
+// hold anything, NaN included). A row whose partials are all empty gives
+// o = 0, lse = -inf.
 //
 // HBM-bound: each partial o_p (D fp32) is read once, each output written
-// once. Lanes of a warp hold consecutive float4 slices of D (coalesced);
-// the warps of a row split the partitions and combine through shared memory.
+// once. One warp per row; lanes hold consecutive float4 slices of D
+// (coalesced).
 #include <math.h>
 
 #include "common.cuh"
@@ -29,87 +30,60 @@ struct RowView {
   int num_parts;
 };
 
-// Merge one row with WPR warps (threads = 32 * WPR). NV = float4 slices per
-// lane (head_dim <= 128 * NV). Writes out_row[0..D) and *out_lse (nullable).
-template <int WPR, int NV>
-__device__ __forceinline__ void merge_row(const RowView& v, int D, float* out_row, float* out_lse,
-                                          float* red /* shared, WPR*(D+2) floats or null */) {
+// Merge one row with one warp. NV = float4 slices per lane (head_dim <=
+// 128 * NV). One pass over the partitions with a running maximum: U
+// partitions' lse and outputs are loaded together before any is used, so a
+// row costs about ceil(P / U) memory round trips instead of P. An empty
+// partition's output is loaded with the others but never enters a sum.
+// Writes out_row[0..D) and *out_lse (nullable).
+template <int NV, int U>
+__device__ __forceinline__ void merge_row(const RowView& v, int D, float* out_row,
+                                          float* out_lse) {
   const int lane = threadIdx.x & 31;
-  const int warp = (WPR == 1) ? 0 : (threadIdx.x >> 5);
-  // max over partitions
-  float M = -INFINITY;
-  for (int p = warp * 32 + lane; p < v.num_parts; p += WPR * 32)
-    M = fmaxf(M, v.lse_base[(int64_t)p * v.lse_stride]);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (WPR > 1) {
-    if (lane == 0) red[warp] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < WPR; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
-  }
   const int nvec = D >> 2;
+  float M = -INFINITY, wsum = 0.f;  // log2 domain
   float4 acc[NV];
 #pragma unroll
   for (int j = 0; j < NV; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int p = warp; p < v.num_parts; p += WPR) {
-      const float l = v.lse_base[(int64_t)p * v.lse_stride];
-      if (l == -INFINITY) continue;
-      const float w = fast_exp2((l - M) * kLog2e);
-      wsum += w;
+  for (int base = 0; base < v.num_parts; base += U) {
+    float l[U];
+    float4 o[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int p = base + u;
+      l[u] = p < v.num_parts ? v.lse_base[(int64_t)p * v.lse_stride] * kLog2e : -INFINITY;
       const float4* op = reinterpret_cast<const float4*>(v.o_base + (int64_t)p * v.o_stride);
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int c = lane + 32 * j;
-        if (c < nvec) {
-          const float4 x = op[c];
-          acc[j].x += w * x.x;
-          acc[j].y += w * x.y;
-          acc[j].z += w * x.z;
-          acc[j].w += w * x.w;
-        }
+        o[u][j] = (p < v.num_parts && c < nvec) ? op[c] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  }
-  if (WPR > 1) {
-    // combine the warps' partial sums: red[w*(D+1) + d], red[w*(D+1) + D] = wsum
-    float* mine = red + warp * (D + 1);
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int c = lane + 32 * j;
-      if (c < nvec) {
-        mine[4 * c] = acc[j].x;
-        mine[4 * c + 1] = acc[j].y;
-        mine[4 * c + 2] = acc[j].z;
-        mine[4 * c + 3] = acc[j].w;
+    for (int u = 0; u < U; ++u) {
+      if (l[u] == -INFINITY) continue;  // empty (or past the last partition)
+      if (l[u] > M) {
+        const float c = fast_exp2(M - l[u]);  // 0 while M is -inf
+        wsum *= c;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          acc[j].x *= c;
+          acc[j].y *= c;
+          acc[j].z *= c;
+          acc[j].w *= c;
+        }
+        M = l[u];
       }
-    }
-    if (lane == 0) mine[D] = wsum;
-    __syncthreads();
-    if (warp == 0) {
-      wsum = 0.f;
-      for (int w = 0; w < WPR; ++w) wsum += red[w * (D + 1) + D];
+      const float w = fast_exp2(l[u] - M);
+      wsum += w;
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
-        const int c = lane + 32 * j;
-        if (c < nvec) {
-          float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int w = 0; w < WPR; ++w) {
-            const float* r = red + w * (D + 1) + 4 * c;
-            s.x += r[0];
-            s.y += r[1];
-            s.z += r[2];
-            s.w += r[3];
-          }
-          acc[j] = s;
-        }
+        acc[j].x += w * o[u][j].x;
+        acc[j].y += w * o[u][j].y;
+        acc[j].z += w * o[u][j].z;
+        acc[j].w += w * o[u][j].w;
       }
     }
-    if (warp != 0) return;
   }
   const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
 #pragma unroll
@@ -119,7 +93,7 @@ __device__ __forceinline__ void merge_row(const RowView& v, int D, float* out_ro
       reinterpret_cast<float4*>(out_row)[c] =
           make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
   }
-  if (out_lse && lane == 0) *out_lse = (wsum > 0.f) ? M + logf(wsum) : -INFINITY;
+  if (out_lse && lane == 0) *out_lse = (wsum > 0.f) ? M * kLn2 + logf(wsum) : -INFINITY;
 }
 
 // Public dense merge: one warp per row, 4 rows per CTA.
@@ -130,7 +104,7 @@ __global__ void __launch_bounds__(128)
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= num_rows) return;
   RowView v{part_out + row * D, part_lse + row, num_rows * D, num_rows, num_parts};
-  merge_row<1, NV>(v, D, out + row * D, out_lse ? out_lse + row : nullptr, nullptr);
+  merge_row<NV, NV == 1 ? 8 : 4>(v, D, out + row * D, out_lse ? out_lse + row : nullptr);
 }
 
 }  // namespace

@@ -218,7 +218,7 @@ def test_public_lse_merge(oracle, P, T, H, D):
     pl = (rng.standard_normal((P, T, H)) * 3).astype(np.float32)
     if P > 1:
         pl[0, 0] = -np.inf          # an empty partition
-        po[0, 0] = np.nan           # ... whose output must not be read
+        po[0, 0] = np.nan           # ... whose output must never enter a sum
         pl[:, -1, -1] = -np.inf     # a row with no keys at all
     ref_o, ref_l = oracle.lse_merge(po.astype(np.float64), pl.astype(np.float64))
     lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
