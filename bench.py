@@ -109,7 +109,7 @@ def attention_launches(w, partition_size: int, ci) -> int:
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("decode_mma.cu", "merge.cu", "common.cuh"):
+    for f in ("decode_mma.cu", "common.cuh"):  # the decode and merge grids' sources
         with open(os.path.join(ROOT, "paged_kv_cache_varlen_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -77,3 +77,24 @@ def test_gqa8_head_dim_64(oracle):
     w = wl.build("cascade_g8", lens, [1] * n, 32, 4, 64, 16, seed=82,
                  shared_prefix=[(list(range(n)), p)])
     check(oracle, w, [(0, n, p)])
+
+
+def test_long_prefixes_and_split_tails(oracle):
+    """Tails longer than one 1024-token partition: the tail pass splits them
+    and merges the pieces in its own merge grid before the prefix segments
+    and the tail are merged; prefixes of 4096 and 1024 tokens (more key
+    segments), plus requests in no group with long contexts."""
+    rng = np.random.default_rng(91)
+    sizes, prefixes = [6, 2], [4096, 1024]
+    lens, sp, groups, first = [], [], [], 0
+    for n, p in zip(sizes, prefixes):
+        lens += list(p + rng.integers(1100, 3000, size=n, endpoint=True))
+        sp.append((list(range(first, first + n)), p))
+        groups.append((first, n, p))
+        first += n
+    lens += list(rng.integers(2500, 5000, size=3, endpoint=True))
+    w = wl.build("cascade_long", lens, [1] * len(lens), 32, 8, 128, 16, seed=92,
+                 shared_prefix=sp)
+    ci = wl.cascade_inputs(w, groups)
+    assert ci["max_tail_len"] > 1024
+    check(oracle, w, groups)
