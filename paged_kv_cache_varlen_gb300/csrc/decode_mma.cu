@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   }
   const int32_t qlen = t1 - t0;
   if (qlen < 1 || qlen > p.decode_max_q) return;  // longer requests run on the prefill kernel
+  if (qlen > p.max_query_len) {  // the grid covers only max_query_len queries' rows
+    if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
+    return;
+  }
   const int row0 = sub * kRows;
   if (row0 >= qlen * group) return;  // no row of this request in the subgroup
   const int rows = min(kRows, qlen * group - row0);  // rows of this CTA

@@ -201,6 +201,18 @@ def test_device_errors_set_status_bits_and_spare_other_requests(oracle):
     lens[2] = 5
     dev.attend(lens=gu.i32_tensor(lens))
     assert dev.dev_status() & gu.pkv.DEV_BAD_LENGTHS
+    # a verification request longer than the max_query_len the call was given
+    wv = wl.build("badq", [40, 300], [1, 3], 32, 8, 128, seed=215)
+    ref_pv = oracle.kv_cache_write(wv.pool, wv.k_new, wv.v_new, wv.slot_mapping)
+    ref_ov, _ = oracle.paged_attention(wv.q, ref_pv, wv.block_table, wv.cu_seqlens, wv.seq_lens,
+                                       wv.scale)
+    devv = gu.DeviceStep(wv)
+    devv.write()
+    outv = torch.full(tuple(devv.q.shape), float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_attention_varlen(devv.q, devv.pool, devv.table, devv.cu, devv.lens, 1,
+                               wv.max_seq_len, out=outv, scale=wv.scale, dev_status=devv.status)
+    assert devv.dev_status() & gu.pkv.DEV_BAD_LENGTHS
+    assert np.max(np.abs(outv.cpu().numpy()[0] - ref_ov[0])) <= gu.ATOL  # request 0 untouched
     # a slot outside the pool
     dev.status.zero_()
     slots = w.slot_mapping.copy()
