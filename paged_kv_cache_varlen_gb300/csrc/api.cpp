@@ -298,12 +298,15 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
 
   const uint64_t D = (uint64_t)head_dim;
   const uint64_t pool_rows = (uint64_t)2 * num_blocks * block_size;
-  // decode: a 16-key box of whole rows (as 128-byte halves, swizzled for
-  // conflict-free ldmatrix)
+  // decode: a 16-key box of whole rows of one KV head, the pool viewed as
+  // [D/64][Hkv][rows][64] (strides 128 B, D*2, Hkv*D*2) so that the box
+  // lands as the 16 keys' first 128-byte halves, then their second halves:
+  // with the 128-byte swizzle, 8 consecutive keys of one half then sit in 8
+  // different bank groups (conflict-free ldmatrix)
   CUtensorMap kv_rows;
-  const uint64_t dims[4] = {64, D / 64, (uint64_t)num_kv_heads, pool_rows};
-  const uint64_t strides[3] = {128, D * 2, (uint64_t)num_kv_heads * D * 2};
-  const uint32_t box[4] = {64, (uint32_t)(D / 64), 1, 16};
+  const uint64_t dims[4] = {64, pool_rows, (uint64_t)num_kv_heads, D / 64};
+  const uint64_t strides[3] = {(uint64_t)num_kv_heads * D * 2, D * 2, 128};
+  const uint32_t box[4] = {64, 16, 1, (uint32_t)(D / 64)};
   if (!encode_4d(&kv_rows, kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return PKV_ERR_CUDA;
   if (pkv::launch_decode_mma(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;

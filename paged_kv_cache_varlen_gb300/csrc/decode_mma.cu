@@ -25,8 +25,9 @@
 //     partition); each K/V byte of a partition is read from HBM once;
 //   * 4 warps, each with SPW private slots; a slot holds one 16-token chunk
 //     of K and of V for this KV head, fetched by one TMA load each (box of
-//     16 rows x head_dim, 128-byte swizzle so that ldmatrix reads of 8 rows
-//     hit different banks) and completed on the slot's mbarrier;
+//     16 rows x head_dim, laid out as the rows' first 128-byte halves then
+//     their second halves, 128-byte swizzle, so that the 8 rows an ldmatrix
+//     reads hit 8 different bank groups) and completed on the slot's mbarrier;
 //   * S = Q K^T: Q is held as A fragments (rows = heads, zero padded), K
 //     rows come in by ldmatrix as B fragments; online softmax in the exp2
 //     domain with lazy rescaling (the running maximum moves only when a score
@@ -80,12 +81,12 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
 }
 
 // Byte offset of 16-byte unit `unit` of row `token` in a 16-row x D tile
-// written by TMA with 128-byte swizzle (tile base 1024-byte aligned): row
-// `token` is D/64 consecutive 128-byte lines; inside line q the unit u sits
-// at u ^ (q % 8).
+// written by TMA with 128-byte swizzle (tile base 1024-byte aligned): the
+// tile holds the 16 rows' first 128-byte halves (lines 0..15), then their
+// second halves (lines 16..31); inside line q the unit u sits at u ^ (q % 8).
 template <int D>
 __device__ __forceinline__ uint32_t swz(int token, int unit) {
-  const int line = token * (D / 64) + (unit >> 3);
+  const int line = (unit >> 3) * kChunk + token;
   return (uint32_t)(line * 128 + (((unit & 7) ^ (line & 7)) << 4));
 }
 
@@ -182,8 +183,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     const int key0 = kbeg + (warp + k * kWarps) * kChunk;
     const int32_t row = id * p.block_size + key0 % p.block_size;
     mbar_arrive_expect_tx(bar, SLOT);
-    tma_load_4d(dst, &kv_map, bar, 0, 0, kvh, row);
-    tma_load_4d(dst + HALF, &kv_map, bar, 0, 0, kvh, row + nrows);
+    tma_load_4d(dst, &kv_map, bar, 0, row, kvh, 0);
+    tma_load_4d(dst + HALF, &kv_map, bar, 0, row + nrows, kvh, 0);
   };
 
   int issued = 0;

@@ -64,8 +64,8 @@ size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t 
 // Decode kernel (query_len == 1 requests): TMA-staged pages, QK^T and PV on
 // the warp-level tensor cores (mma.sync); split-KV partitions merged by a
 // second, small grid launched behind it. `kv_map` views the pool as
-// [2*NB*BS rows][Hkv][D/64][64] with a box of {64, D/64, 1, 16} and 128-byte
-// swizzle. Up to 16 query heads per CTA.
+// [D/64][Hkv][2*NB*BS rows][64] (strides 128 B, D*2, Hkv*D*2) with a box of
+// {64, 16, 1, D/64} and 128-byte swizzle. Up to 16 query heads per CTA.
 cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
                               cudaStream_t stream);
 
