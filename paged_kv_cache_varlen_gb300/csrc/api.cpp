@@ -93,9 +93,9 @@ bool resolve_partition(int32_t max_seq_len, int32_t partition_size, int32_t* ps,
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: partial outputs [B][P][H][D] fp32, partial lse [B][P][H] fp32,
-// arrival counters [B][H] int32 (split-KV only), then the prefill work
-// tickets (256 bytes, always); counters and tickets are zero between calls.
+// Workspace: partial outputs [B][P][H][D] fp32 and partial lse [B][P][H]
+// fp32 (split-KV only), then the prefill work tickets (256 bytes, always),
+// which are zero between calls.
 constexpr size_t kSchedBytes = 256;
 
 struct WorkspaceLayout {
