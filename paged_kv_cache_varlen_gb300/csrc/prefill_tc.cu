@@ -512,12 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PrefillItem d = prefill_item(p, pref, QP, it);
         const int n = d.n_tiles;
         ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
-        // S_x is free once PV of the previous item's last tile has completed
-        for (int x = 0; ok && x < kQT; ++x) {
-          if (gt > 0) ok = wait(&bars->o_done[x], (gt - 1) & 1);
-          if (!ok) break;
-          issue_qk(x, gt);
-        }
+        // S_x is reused after PV of the previous item's last tile: in issue order
+        for (int x = 0; ok && x < kQT; ++x) issue_qk(x, gt);
         if (!ok) break;
         if (n == 1) umma_commit(smem_addr(&bars->q_empty));  // Q of this item no longer read
         for (int j = 0; ok && j < n; ++j) {
@@ -531,9 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             issue_pv(x, g, j == 0);
             if (j + 1 < n) {
-              // S_x holds P_x(j) until this PV completes
-              ok = wait(&bars->o_done[x], g & 1) &&
-                   wait(&bars->k_full[(g + 1) % kNS], ((g + 1) / kNS) & 1);
+              // S_x holds P_x(j) until this PV has read it: tcgen05.mma
+              // operations issued by one thread run in issue order, so the
+              // next QK^T into S_x may follow the PV at once
+              ok = wait(&bars->k_full[(g + 1) % kNS], ((g + 1) / kNS) & 1);
               if (!ok) break;
               issue_qk(x, g + 1);
               if (x == kQT - 1 && j + 2 == n) umma_commit(smem_addr(&bars->q_empty));
