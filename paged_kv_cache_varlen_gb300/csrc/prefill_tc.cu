@@ -312,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < kQT; ++x) {
       mbar_init(smem_addr(&bars->s_full[x]), 1);
-      mbar_init(smem_addr(&bars->p_ready[x]), kBM);
+      mbar_init(smem_addr(&bars->p_ready[x]), kBM / 32);  // one arrival per softmax warp
       mbar_init(smem_addr(&bars->o_done[x]), 1);
-      mbar_init(smem_addr(&bars->o_free[x]), kBM);
+      mbar_init(smem_addr(&bars->o_free[x]), kBM / 32);
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
     for (int k = 0; k < kRing; ++k) {
@@ -688,7 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_addr(&bars->p_ready[x]));
+        __syncwarp();  // the warp's P (and O) stores precede its one arrival
+        if (lane == 0) mbar_arrive(smem_addr(&bars->p_ready[x]));
       }
       if (!ok) break;
       // ---- epilogue of the item: O / l -> out, lse
@@ -717,7 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.out_lse[d.seg * p.split_lse_stride + (int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g] =
             (m + fast_log2(l)) * kLn2;
       tc_fence_before();
-      mbar_arrive(smem_addr(&bars->o_free[x]));  // the MMA may overwrite O_x now
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bars->o_free[x]));  // the MMA may overwrite O_x now
       gt += d.n_tiles;
     }
   }
