@@ -107,6 +107,29 @@ def attention_launches(w, partition_size: int, ci) -> int:
     return n
 
 
+def pack_inputs(tensors: dict, align: int = 256):
+    """Lay contiguous tensors end to end in one byte buffer, each piece at an
+    `align`-byte offset. Returns ({name: (offset, bytes)}, total bytes, the
+    packed uint8 tensor)."""
+    import torch
+
+    offs, total = {}, 0
+    for k, v in tensors.items():
+        offs[k] = (total, v.numel() * v.element_size())
+        total = -(-(total + offs[k][1]) // align) * align
+    buf = torch.zeros(total, dtype=torch.uint8)
+    for k, v in tensors.items():
+        o, n = offs[k]
+        buf[o:o + n].copy_(v.reshape(-1).view(torch.uint8))
+    return offs, total, buf
+
+
+def unpack_views(buf, offs: dict, like: dict) -> dict:
+    """Views of a packed byte buffer with the dtypes and shapes of `like`."""
+    return {k: buf[o:o + n].view(like[k].dtype).view(like[k].shape)
+            for k, (o, n) in offs.items()}
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("decode_mma.cu", "common.cuh"):  # the decode and merge grids' sources
@@ -357,22 +380,14 @@ def run_ours(args):
         host["table"] = torch.from_numpy(w.block_table).pin_memory()
         host["cu"] = torch.from_numpy(w.cu_seqlens).pin_memory()
         host["lens"] = torch.from_numpy(w.seq_lens).pin_memory()
-    # every per-step input packed into one pinned host buffer (256-byte
-    # aligned pieces), so that a step's inputs travel in one copy
-    offs, total_in = {}, 0
-    for k, v in host.items():
-        offs[k] = (total_in, v.numel() * v.element_size())
-        total_in = -(-(total_in + offs[k][1]) // 256) * 256
-    host_buf = torch.empty(total_in, dtype=torch.uint8).pin_memory()
-    for k, v in host.items():
-        o, n = offs[k]
-        host_buf[o:o + n].copy_(v.reshape(-1).view(torch.uint8))
+    # every per-step input packed into one pinned host buffer, so that a
+    # step's inputs travel in one copy
+    offs, total_in, host_buf = pack_inputs(host)
+    host_buf = host_buf.pin_memory()
 
     def device_set():
         buf = torch.empty(total_in, dtype=torch.uint8, device=dev)
-        views = {k: buf[o:o + n].view(host[k].dtype).view(host[k].shape)
-                 for k, (o, n) in offs.items()}
-        return buf, views
+        return buf, unpack_views(buf, offs, host)
 
     d_buf, d = device_set()
     d_buf.copy_(host_buf)

@@ -113,3 +113,24 @@ def test_split_parts_follows_the_library():
             rows = B * n * H
             want = 256 if n == 1 else up(rows * D * 4) + up(rows * 4) + 256
             assert ws == want, (L, ps, n, ws, want)
+
+
+def test_packed_inputs_round_trip():
+    """The end-to-end step copies all of its inputs in one packed buffer;
+    the views bench.py hands to the kernels must hold exactly the inputs,
+    at 256-byte aligned offsets (the kernels need 16-byte alignment)."""
+    import torch
+    rng = np.random.default_rng(3)
+    host = {
+        "q": torch.from_numpy(rng.integers(-2**15, 2**15, size=(5, 4, 64), dtype=np.int16)
+                              ).view(torch.bfloat16),
+        "slots": torch.from_numpy(rng.integers(0, 1000, size=7, dtype=np.int32)),
+        "table": torch.from_numpy(rng.integers(0, 1000, size=(3, 9), dtype=np.int32)),
+        "cu": torch.from_numpy(np.array([0, 2, 5, 7], dtype=np.int32)),
+    }
+    offs, total, buf = bench.pack_inputs(host)
+    assert total % 256 == 0 and all(o % 256 == 0 for o, _ in offs.values())
+    views = bench.unpack_views(buf.clone(), offs, host)
+    for k, v in host.items():
+        assert views[k].dtype == v.dtype and views[k].shape == v.shape
+        assert torch.equal(views[k].view(torch.uint8), v.view(torch.uint8)), k
