@@ -32,7 +32,7 @@ struct AttnParams {
   int32_t num_seqs, num_tokens, max_query_len, max_seq_len;
   int32_t num_heads, num_kv_heads, head_dim, block_size, num_blocks;
   float scale_log2;           // scale * log2(e)
-  // split-KV for query_len == 1 requests
+  // split-KV for query_len == 1 requests (merged by the decode merge grid)
   int32_t part_size;          // tokens per partition (multiple of 16)
   int32_t num_parts;          // partitions per request covering max_seq_len
   float* ws_out;              // [B][num_parts][H][D] (null when num_parts == 1)
@@ -40,15 +40,15 @@ struct AttnParams {
   int32_t* sched;             // prefill work tickets: [0] next item, [1] CTAs done;
                               // zero between calls
   int32_t* status;
-  // shared-prefix (cascade) pass of the prefill kernel: every query of a
-  // "request" (a prefix group) sees all seq_len keys, no causal mask; the
-  // keys are cut into at most kv_splits segments, segment s writing its
-  // normalised partial to out + s * split_out_stride and its lse to
-  // out_lse + s * split_lse_stride
   // requests of 1 .. decode_max_q queries run on the decode kernel (its MMA
   // rows are (query, head) pairs, at most decode_max_rows per request in the
   // launch); longer ones on the prefill kernel
   int32_t decode_max_q, decode_max_rows;
+  // shared-prefix (cascade) pass of the prefill kernel (prefix_mode 1):
+  // every query of a "request" (a prefix group) sees all seq_len keys, no
+  // causal mask; the keys are cut into at most kv_splits segments, segment s
+  // writing its normalised partial to out + s * split_out_stride and its lse
+  // to out_lse + s * split_lse_stride
   int32_t prefix_mode;        // 0: ordinary causal prefill
   int32_t kv_splits;
   int64_t split_out_stride, split_lse_stride;
