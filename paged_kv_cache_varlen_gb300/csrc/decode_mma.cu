@@ -366,15 +366,16 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   l1 += __shfl_xor_sync(kFull, l1, 2);
 
   __syncthreads();  // every warp is done with its slots: reuse them
-  float* red_o = reinterpret_cast<float*>(smem);       // [kWarps][kRows][D]
-  float* red_ml = red_o + kWarps * kRows * D;          // [kWarps][kRows][2]
+  // rows padded to D + 8 floats: the quads of 4 consecutive rows store to
+  // disjoint banks; rows past the CTA's own are not stored at all
+  constexpr int RS = D + 8;
+  float* red_o = reinterpret_cast<float*>(smem);       // [kWarps][kRows][RS]
+  float* red_ml = red_o + kWarps * kRows * RS;         // [kWarps][kRows][2]
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float* dst = red_o + (warp * kRows + r) * D + nt * 8 + cq;
-    dst[0] = o[nt][0];
-    dst[1] = o[nt][1];
-    dst[8 * D] = o[nt][2];
-    dst[8 * D + 1] = o[nt][3];
+    float* dst = red_o + (warp * kRows + r) * RS + nt * 8 + cq;
+    if (r < rows) *reinterpret_cast<float2*>(dst) = make_float2(o[nt][0], o[nt][1]);
+    if (r + 8 < rows) *reinterpret_cast<float2*>(dst + 8 * RS) = make_float2(o[nt][2], o[nt][3]);
   }
   if ((lane & 3) == 0) {
     red_ml[(warp * kRows + r) * 2] = m0;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       if (mw == -INFINITY) continue;
       const float a = fast_exp2(mw - M);
       wsum += a * red_ml[(w * kRows + g) * 2 + 1];
-      acc += a * red_o[(w * kRows + g) * D + d];
+      acc += a * red_o[(w * kRows + g) * RS + d];
     }
     const float val = wsum > 0.f ? acc / wsum : 0.f;
     const float lse = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
