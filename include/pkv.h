@@ -14,7 +14,10 @@
  * ---------------------------------------
  * - All tensor pointers are DEVICE pointers owned by the caller. The library
  *   never allocates device memory, never frees it, never synchronises the
- *   stream and keeps no state between calls.
+ *   stream and keeps no state between calls, with two stated exceptions: the
+ *   built-in scratch array of pkv_paged_attention_varlen_noalloc and the
+ *   host-side block manager objects (pkv_bm_*), which the caller creates and
+ *   destroys.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream). A call returns as soon as the
  *   kernels are queued.
