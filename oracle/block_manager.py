@@ -19,7 +19,7 @@ deep-dive", the block-table and copy-on-write passages):
 * a shared block gets its own copy only when a sequence writes into it:
   "write-time allocation" of a new block for the sequence that diverges.
 
-Readings where the page is silent (listed in the design doc as well):
+Readings where the page is silent:
 
 * free-pool order: first in, first out, starting from ``free_order`` (default
   ascending ids); a released block joins the back of the queue;
