@@ -129,3 +129,40 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
     with pytest.raises(binding.PkvError):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_cascade_workspace_size_arithmetic(lib):
+    up = lambda x: -(-x // 256) * 256
+    B, H, Hkv, D = 256, 32, 8, 128
+
+    def expect(splits, tail_parts):
+        rows = (splits + 1) * B * H          # S prefix segments, then the tail
+        size = up(rows * D * 4) + up(rows * 4) + up((B + 1) * 4)
+        if tail_parts > 1:                   # the tail pass's own split-KV partials
+            trows = B * tail_parts * H
+            size += up(trows * D * 4) + up(trows * 4)
+        return size + 256                    # prefill work tickets
+    # 4 groups of 64 members, 2048-token prefixes: 64 queries per work item at
+    # G = 4, so 4 x 1 x 8 = 32 items; ceil(148 / 32) = 5 key segments
+    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 1024, H, Hkv, D) == expect(5, 1)
+    # tails up to 3000 tokens split into 3 partitions of 1024
+    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 3000, H, Hkv, D) == expect(5, 3)
+    # no groups: one (empty) prefix slot and the tail
+    assert lib.pkv_cascade_workspace_size(B, 0, 1, 0, 1024, H, Hkv, D) == expect(1, 1)
+    # segments never outnumber the prefix's 128-key tiles (256 tokens: 2 tiles)
+    assert lib.pkv_cascade_workspace_size(B, 1, 4, 256, 1024, H, Hkv, D) == expect(2, 1)
+    # invalid sizes
+    assert lib.pkv_cascade_workspace_size(0, 4, 64, 2048, 1024, H, Hkv, D) == 0
+    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 1024, 30, Hkv, D) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, 16, 16, -1, 8, 16, 2, 128, None, None), 1),     # negative count
+    ((16, 16, 16, 0, 8, 16, 2, 128, None, None), 0),      # nothing to copy
+    ((None, 16, 16, 2, 8, 16, 2, 128, None, None), 1),    # no pool
+    ((24, 16, 16, 2, 8, 16, 2, 128, None, None), 1),      # pool not 16-byte aligned
+    ((16, None, 16, 2, 8, 16, 2, 128, None, None), 1),    # no source list
+    ((16, 16, 16, 2, 0, 16, 2, 128, None, None), 1),      # empty pool
+])
+def test_copy_blocks_rejects_before_launch(lib, args, status):
+    assert lib.pkv_copy_blocks(*args) == status
