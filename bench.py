@@ -51,6 +51,9 @@ def parse_args():
                     help="prefix_cow only: read each shared prefix once per group "
                          "(pkv_cascade_decode) instead of once per request")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--extra", default=EXTRA_DEFAULT,
+                    help="comma-separated workloads also timed device-resident in the same "
+                         "run and reported under 'workloads' ('none' to skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target length of the oracle CPU-baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
@@ -154,14 +157,17 @@ def profiled_traffic(config: str):
 
 
 class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms while the
+    timed work runs. The median SM clock is taken over the samples that saw
+    the GPU busy (utilization >= 50 %), so idle gaps do not pull it down."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
-        self.lines = []
 
     def start(self):
         try:
@@ -172,32 +178,55 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
+    @staticmethod
+    def summarise(text: str) -> dict:
+        sm, smax, busy, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in text.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                mhz, mx, util = float(parts[1]), float(parts[2]), float(parts[9])
+            except ValueError:
+                continue
+            sm.append(mhz)
+            smax.append(mx)
+            if util >= 50.0:
+                busy.append(mhz)
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        pick = busy if busy else sm
+        return {"sm_mhz": statistics.median(pick) if pick else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_under_load": len(busy)}
+
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_under_load": 0}
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarise(out)
+
+
+def l2_size(device=None) -> int:
+    """L2 bytes of the GPU (both arms report the same figure on one box)."""
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(device if device is not None else 0)
+                       .L2_cache_size)
+    except Exception:
+        pass
+    return 126 * 2**20
 
 
 def dist_info():
@@ -349,7 +378,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "seqs_per_s": sample.num_seqs / sec,
         "config": workload_config(w, args.partition_size, world,
-                                  pool_copies(w.kv_bytes(), 126 * 2**20)),
+                                  pool_copies(w.kv_bytes(), l2_size()), l2_size()),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{desc} of the rank-0 batch, every step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -358,12 +387,154 @@ def run_reference(args):
     return 0
 
 
+EXTRA_DEFAULT = "long_split_kv,spec_verify,mixed_step"
+
+
+class DeviceWorkload:
+    """One rank's batch of a workload resident on its GPU: the packed per-step
+    inputs (pinned on the host and on the device), the KV pool (rotated over
+    copies when a step's KV read is smaller than twice the L2), the outputs
+    and the workspace, and the calls of one step."""
+
+    def __init__(self, w, dev, stream, partition_size: int, cascade: bool, l2_bytes: int):
+        import torch
+
+        from paged_kv_cache_varlen_gb300 import binding as pkv
+        from paged_kv_cache_varlen_gb300 import workloads as wl
+
+        self.w, self.dev, self.stream, self.pkv = w, dev, stream, pkv
+        self.partition_size = partition_size
+        T, H, D = w.q.shape
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+        host = {"q": bf16(w.q), "k_new": bf16(w.k_new), "v_new": bf16(w.v_new),
+                "slots": torch.from_numpy(w.slot_mapping)}
+        self.ci = None
+        if cascade:
+            if "prefix_tokens" not in w.meta:
+                raise SystemExit("--cascade needs a workload with shared prefixes (prefix_cow)")
+            self.ci = wl.cascade_inputs(w, wl.prefix_groups(w))
+            for k in ("group_starts", "prefix_lens", "prefix_tables", "tail_tables",
+                      "tail_lens"):
+                host[k] = torch.from_numpy(self.ci[k])
+        else:
+            host["table"] = torch.from_numpy(w.block_table)
+            host["cu"] = torch.from_numpy(w.cu_seqlens)
+            host["lens"] = torch.from_numpy(w.seq_lens)
+        # every per-step input packed into one pinned host buffer, so that a
+        # step's inputs travel in one copy
+        self.host = host
+        self.offs, self.total_in, buf = pack_inputs(host)
+        self.host_buf = buf.pin_memory()
+        self.d_buf, self.d = self.device_set()
+        self.d_buf.copy_(self.host_buf)
+        pool = bf16(w.pool).to(dev)
+        unique = w.unique_kv_bytes() if "prefix_tokens" in w.meta else w.kv_bytes()
+        self.n_pools = pool_copies(unique, l2_bytes)
+        self.pools = [pool] + [pool.clone() for _ in range(self.n_pools - 1)]
+        self.out = torch.empty((T, H, D), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        if self.ci is not None:
+            ci = self.ci
+            ws_bytes = pkv.cascade_workspace_size(w.num_seqs, len(ci["prefix_lens"]),
+                                                  ci["max_group_size"], ci["max_prefix_len"],
+                                                  ci["max_tail_len"], H, w.num_kv_heads, D)
+        else:
+            ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D,
+                                                    w.max_seq_len, partition_size)
+        self.ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def device_set(self):
+        import torch
+
+        buf = torch.empty(self.total_in, dtype=torch.uint8, device=self.dev)
+        return buf, unpack_views(buf, self.offs, self.host)
+
+    def attend(self, dd=None, ev=None, res=None, k=0):
+        w, pkv, ci = self.w, self.pkv, self.ci
+        dd = self.d if dd is None else dd
+        o, ls = (self.out, self.lse) if res is None else res
+        pool = self.pools[k % self.n_pools]
+        if ev is not None:
+            ev[0].record(self.stream)
+        if ci is not None:
+            pkv.cascade_decode(dd["q"], pool, dd["group_starts"], dd["prefix_lens"],
+                               dd["prefix_tables"], ci["max_group_size"], ci["max_prefix_len"],
+                               dd["tail_tables"], dd["tail_lens"], ci["max_tail_len"], out=o,
+                               out_lse=ls, scale=w.scale, workspace=self.ws, stream=self.stream)
+        else:
+            pkv.paged_attention_varlen(dd["q"], pool, dd["table"], dd["cu"], dd["lens"],
+                                       w.max_query_len, w.max_seq_len, out=o, out_lse=ls,
+                                       scale=w.scale, partition_size=self.partition_size,
+                                       workspace=self.ws, stream=self.stream)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def step(self, dd=None, res=None, k=0):
+        dd = self.d if dd is None else dd
+        self.pkv.kv_cache_write(self.pools[k % self.n_pools], dd["k_new"], dd["v_new"],
+                                dd["slots"], stream=self.stream)
+        self.attend(dd, res=res, k=k)
+
+    def timed(self, fn, K: int) -> float:
+        """ms of K calls of fn(k) back to back between one pair of events (an
+        event recorded between two kernels would also stop the next one from
+        launching early under programmatic dependent launch)."""
+        import torch
+
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        a.record(self.stream)
+        for k in range(K):
+            fn(k)
+        b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return a.elapsed_time(b)
+
+    def launches_per_step(self) -> int:
+        return 1 + attention_launches(self.w, self.partition_size, self.ci)
+
+
+def roofline_and_prefill(w, attn_avg_ms: float, ci=None) -> tuple:
+    """(roofline, prefill) objects of one workload's attention call: KV bytes
+    over the call's time against the measured HBM peak (unique bytes for
+    shared prefixes), and for batches with requests on the tensor-core
+    prefill kernel their causal-exact TFLOP/s and the serial bound T*."""
+    peak, peak_kind = hbm_peak()
+    kv_bytes = w.kv_bytes()
+    roof_bytes = w.unique_kv_bytes() if "prefix_tokens" in w.meta else kv_bytes
+    achieved = roof_bytes / (attn_avg_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm",
+            "kernel": ("cascade call (prefix pass + tail decode + merge)" if ci is not None
+                       else "attention call (decode + split-KV merge"
+                       + (" + prefill)" if w.max_query_len > max(1, 32 // (
+                           w.num_heads // w.num_kv_heads)) else ")")),
+            "bytes_per_call": roof_bytes, "achieved": achieved, "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak}
+    dmq = max(1, 32 // (w.num_heads // w.num_kv_heads))
+    flops = w.attention_flops(dmq + 1)
+    prefill = None
+    if flops > 0:
+        tpeak, tkind = tensor_peak()
+        tflops = flops / (attn_avg_ms * 1e-3) / 1e12
+        # serial bound of the whole call: every K/V byte at the HBM peak plus
+        # the prefill FLOPs at the tensor peak
+        t_star_us = 1e6 * (kv_bytes / (peak * 1e9) + flops / (tpeak * 1e12))
+        prefill = {"flops_per_step": flops, "achieved_tflops": tflops, "peak_tflops": tpeak,
+                   "peak_kind": tkind, "frac": tflops / tpeak, "t_star_us": t_star_us,
+                   "t_star_frac": t_star_us / (attn_avg_ms * 1e3),
+                   "time": "attention call" + (" (decode kernel included)"
+                                               if (w.query_lens <= dmq).any() else "")}
+    return roof, prefill
+
+
 def run_ours(args):
     import torch
 
     from paged_kv_cache_varlen_gb300 import binding as pkv
     from paged_kv_cache_varlen_gb300 import build as pkv_build
-    from paged_kv_cache_varlen_gb300 import workloads as wl
 
     world, rank, local = dist_info()
     if not torch.cuda.is_available():
@@ -377,130 +548,49 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     pkv_build.build()
     pkv.load_library()
+    stream = torch.cuda.current_stream(dev)
+    l2_bytes = l2_size(dev)
 
     w = rank_workload(args.config, rank)
     T, H, D = w.q.shape
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-
-    host = {
-        "q": bf16(w.q).pin_memory(), "k_new": bf16(w.k_new).pin_memory(),
-        "v_new": bf16(w.v_new).pin_memory(),
-        "slots": torch.from_numpy(w.slot_mapping).pin_memory(),
-    }
-    ci = None
-    if args.cascade:
-        if "prefix_tokens" not in w.meta:
-            raise SystemExit("--cascade needs a workload with shared prefixes (prefix_cow)")
-        ci = wl.cascade_inputs(w, wl.prefix_groups(w))
-        for k in ("group_starts", "prefix_lens", "prefix_tables", "tail_tables", "tail_lens"):
-            host[k] = torch.from_numpy(ci[k]).pin_memory()
-    else:
-        host["table"] = torch.from_numpy(w.block_table).pin_memory()
-        host["cu"] = torch.from_numpy(w.cu_seqlens).pin_memory()
-        host["lens"] = torch.from_numpy(w.seq_lens).pin_memory()
-    # every per-step input packed into one pinned host buffer, so that a
-    # step's inputs travel in one copy
-    offs, total_in, host_buf = pack_inputs(host)
-    host_buf = host_buf.pin_memory()
-
-    def device_set():
-        buf = torch.empty(total_in, dtype=torch.uint8, device=dev)
-        return buf, unpack_views(buf, offs, host)
-
-    d_buf, d = device_set()
-    d_buf.copy_(host_buf)
-    pool = bf16(w.pool).to(dev)
-    try:
-        l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
-    except Exception:
-        l2_bytes = 126 * 2**20
-    unique = w.unique_kv_bytes() if "prefix_tokens" in w.meta else w.kv_bytes()
-    n_pools = pool_copies(unique, l2_bytes)
-    pools = [pool] + [pool.clone() for _ in range(n_pools - 1)]
-    out = torch.empty((T, H, D), dtype=torch.float32, device=dev)
-    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    if ci is not None:
-        ws_bytes = pkv.cascade_workspace_size(w.num_seqs, len(ci["prefix_lens"]),
-                                              ci["max_group_size"], ci["max_prefix_len"],
-                                              ci["max_tail_len"], H, w.num_kv_heads, D)
-    else:
-        ws_bytes = pkv.attention_workspace_size(w.num_seqs, T, H, w.num_kv_heads, D,
-                                                w.max_seq_len, args.partition_size)
-    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def attend_only(dd, ev=None, res=None, k=0):
-        o, ls = (out, lse) if res is None else res
-        pool = pools[k % n_pools]
-        if ev is not None:
-            ev[0].record(stream)
-        if ci is not None:
-            pkv.cascade_decode(dd["q"], pool, dd["group_starts"], dd["prefix_lens"],
-                               dd["prefix_tables"], ci["max_group_size"], ci["max_prefix_len"],
-                               dd["tail_tables"], dd["tail_lens"], ci["max_tail_len"], out=o,
-                               out_lse=ls, scale=w.scale, workspace=ws, stream=stream)
-        else:
-            pkv.paged_attention_varlen(dd["q"], pool, dd["table"], dd["cu"], dd["lens"],
-                                       w.max_query_len, w.max_seq_len, out=o, out_lse=ls,
-                                       scale=w.scale, partition_size=args.partition_size,
-                                       workspace=ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    def step(dd, res=None, k=0):
-        pkv.kv_cache_write(pools[k % n_pools], dd["k_new"], dd["v_new"], dd["slots"],
-                           stream=stream)
-        attend_only(dd, res=res, k=k)
-
-    dev_args = (d,)
-    for k in range(max(3, args.warmup)):
-        step(*dev_args, k=k)
+    R = DeviceWorkload(w, dev, stream, args.partition_size, args.cascade, l2_bytes)
+    W = max(3, args.warmup)
+    for k in range(W):
+        R.step(k=k)
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timed region -------------------------------------
-    # The K steps run back to back with events only around the whole region:
-    # an event recorded between two kernels would also stop the next kernel
-    # from launching early (programmatic dependent launch), which costs ~8 us
-    # per step on the Llama decode shape.
-    K = args.steps
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a_start, a_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = str(local)
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
+    # untimed steps for ~0.4 s before the timed region, so that the clock
+    # sampler sees the GPU under this load
+    soak_steps, t_soak = 0, time.perf_counter()
+    while time.perf_counter() - t_soak < 0.4:
+        for k in range(50):
+            R.step(k=k)
+        soak_steps += 50
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region -------------------------------------
+    K = args.steps
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for k in range(K):
-        step(*dev_args, k=k)
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms = R.timed(lambda k: R.step(k=k), K)
     # the attention call alone, K calls back to back (the roofline's kernel
     # time: its average launch duration over this region)
-    a_start.record(stream)
-    for k in range(K):
-        attend_only(*dev_args, k=k)
-    a_stop.record(stream)
-    torch.cuda.synchronize(dev)
+    attn_avg_ms = R.timed(lambda k: R.attend(k=k), K) / K
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
-    total_ms = start.elapsed_time(stop)
-    attn_avg_ms = a_start.elapsed_time(a_stop) / K
     # spread of single calls, each between its own pair of events (which
     # serialise it against its neighbours, so these run a little longer)
     NP = min(K, 200)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(NP)]
     for k in range(NP):
-        attend_only(*dev_args, ev=evs[k], k=k)
+        R.attend(ev=evs[k], k=k)
     torch.cuda.synchronize(dev)
     attn_ms = [a.elapsed_time(b) for a, b in evs]
 
@@ -509,13 +599,14 @@ def run_ours(args):
     # its output back, pipelined the way a serving loop runs: two device
     # buffer sets, the inputs of step k+1 copied (one stream) and the output
     # of step k-1 read back (another) while step k's kernels run; the steps'
-    # kernels stay in order on the compute stream (they share the pool).
-    E = args.e2e_steps if args.e2e_steps is not None else max(3, K // 4)
+    # kernels stay in order on the compute stream (they share the pool). At
+    # least 200 steps, so that the pipeline's fill does not set the figure.
+    E = args.e2e_steps if args.e2e_steps is not None else max(200, K // 4)
     E = max(E, 1)
-    bufs = [(d_buf, d), device_set()]
-    results = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
+    bufs = [(R.d_buf, R.d), R.device_set()]
+    results = [(R.out, R.lse), (torch.empty_like(R.out), torch.empty_like(R.lse))]
     out_hosts = [torch.empty((T, H, D), dtype=torch.float32).pin_memory() for _ in range(2)]
-    h2d = total_in
+    h2d = R.total_in
     d2h = out_hosts[0].numel() * out_hosts[0].element_size()
     copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     landed = [torch.cuda.Event(), torch.cuda.Event()]   # inputs of the set copied in
@@ -533,12 +624,12 @@ def run_ours(args):
         if k >= 2:
             copy_in.wait_event(used[sb])
         with torch.cuda.stream(copy_in):
-            bufs[sb][0].copy_(host_buf, non_blocking=True)
+            bufs[sb][0].copy_(R.host_buf, non_blocking=True)
         landed[sb].record(copy_in)
         stream.wait_event(landed[sb])
         if k >= 2:
             stream.wait_event(read[sb])
-        step(bufs[sb][1], res=results[sb], k=k)
+        R.step(bufs[sb][1], res=results[sb], k=k)
         used[sb].record(stream)
         copy_out.wait_event(used[sb])
         with torch.cuda.stream(copy_out):
@@ -550,6 +641,39 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_stop)
 
+    # ---- the other workloads of the hot path, device-resident --------------
+    extras = {}
+    extra_names = [] if args.extra in ("", "none") else args.extra.split(",")
+    for name in extra_names:
+        if name == args.config:
+            continue
+        del bufs, results
+        torch.cuda.empty_cache()
+        we = rank_workload(name, rank)
+        RE = DeviceWorkload(we, dev, stream, -1, False, l2_bytes)
+        for k in range(W):
+            RE.step(k=k)
+        if dist is not None:
+            dist.barrier()
+        e_total = RE.timed(lambda k: RE.step(k=k), K)
+        e_attn = RE.timed(lambda k: RE.attend(k=k), K)
+        t = max_over_ranks({"total_ms": e_total, "attn_ms": e_attn}, dist, dev)
+        step_ms, attn_e_ms = t["total_ms"] / K, t["attn_ms"] / K
+        roof, pre = roofline_and_prefill(we, attn_e_ms)
+        extras[name] = {
+            "num_seqs": we.num_seqs, "num_tokens": we.num_tokens,
+            "kv_bytes_per_step": we.kv_bytes(), "step_us": step_ms * 1e3,
+            "kv_gbs": job_throughput(world, we.kv_bytes(), step_ms),
+            "seqs_per_s": world * we.num_seqs / (step_ms * 1e-3),
+            "query_tokens_per_s": world * we.num_tokens / (step_ms * 1e-3),
+            "attention_us": attn_e_ms * 1e3, "roofline": roof, "prefill": pre,
+            "l2": workload_config(we, -1, world, RE.n_pools, l2_bytes)["l2"],
+            "gpu_launches": RE.launches_per_step() * K + (RE.launches_per_step() - 1) * K}
+        del RE, we
+        bufs, results = None, None
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+
     # ---- reduce over ranks --------------------------------------------------
     slowest = max_over_ranks({"total_ms": total_ms, "e2e_ms": e2e_ms, "attn_avg_ms": attn_avg_ms},
                              dist, dev)
@@ -559,29 +683,9 @@ def run_ours(args):
     ms_per_step = total_ms / K
     value = job_throughput(world, kv_bytes, ms_per_step)
     e2e_value = job_throughput(world, kv_bytes, e2e_ms / E)
-    peak, peak_kind = hbm_peak()
-    # shared prefixes: the roofline counts every physical byte once (a prefix
-    # may legitimately be served from L2, or be read once per group)
-    roof_bytes = w.unique_kv_bytes() if "prefix_tokens" in w.meta else kv_bytes
-    achieved = roof_bytes / (attn_avg_ms * 1e-3) / 1e9
-    launches_per_step = 1 + attention_launches(w, args.partition_size, ci)
-    prefill_line = None
-    # requests longer than the decode kernel takes (32 / G queries) run on the
-    # tensor-core prefill kernel; the attention call also holds the decode
-    # kernel when the batch has decodes or verification steps
-    dmq = max(1, 32 // (w.num_heads // w.num_kv_heads))
-    flops = w.attention_flops(dmq + 1)
-    if flops > 0:
-        tpeak, tkind = tensor_peak()
-        tflops = flops / (attn_avg_ms * 1e-3) / 1e12
-        # serial bound of the whole call: every K/V byte at the HBM peak plus
-        # the prefill FLOPs at the tensor peak
-        t_star_us = 1e6 * (kv_bytes / (peak * 1e9) + flops / (tpeak * 1e12))
-        prefill_line = {"flops_per_step": flops, "achieved_tflops": tflops, "peak_tflops": tpeak,
-                        "peak_kind": tkind, "frac": tflops / tpeak,
-                        "t_star_us": t_star_us, "t_star_frac": t_star_us / (attn_avg_ms * 1e3),
-                        "time": "attention call" + (" (decode kernel included)"
-                                                    if (w.query_lens <= dmq).any() else "")}
+    peak, _ = hbm_peak()
+    roof, prefill_line = roofline_and_prefill(w, attn_avg_ms, R.ci)
+    roof["traffic"] = profiled_traffic(args.config)
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         sample, desc = oracle_sample(w)
@@ -593,9 +697,12 @@ def run_ours(args):
                "single_core": {"value": sample.kv_bytes() / sec1 / 1e9, "unit": "GB/s",
                                "steps": n1}}
     if rank == 0:
+        # the headline step (K) and attention calls (K), single calls (NP) and
+        # e2e steps (E), plus each extra workload's K steps and K calls
+        launches = R.launches_per_step()
         line = {
             "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
-            "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+            "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
@@ -609,26 +716,21 @@ def run_ours(args):
                                  "p50": 1e3 * float(np.percentile(attn_ms, 50)),
                                  "p90": 1e3 * float(np.percentile(attn_ms, 90))}},
             "pct_of_hbm_peak": 100.0 * value / world / peak,
-            "config": workload_config(w, args.partition_size, world, n_pools, l2_bytes),
-            "roofline": {"bound": "hbm",
-                         "kernel": ("cascade call (prefix pass + tail decode + merge)"
-                                    if ci is not None else
-                                    "attention call (decode + split-KV merge)"),
-                         "bytes_per_call": roof_bytes,
-                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": profiled_traffic(args.config)},
+            "config": workload_config(w, args.partition_size, world, R.n_pools, l2_bytes),
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": e2e_ms / E,
                     "copies": "pinned host, one copy of all inputs in and one of the output "
                               "out per step; step k+1's inputs and step k-1's output move "
                               "while step k runs (two device buffer sets)"},
             "prefill": prefill_line,
-            "gpu_launches": launches_per_step * K,
-            "clocks": clocks,
+            "gpu_launches": (launches * K + (launches - 1) * (K + NP) + launches * E
+                             + sum(x["gpu_launches"] for x in extras.values())),
+            "workloads": extras,
+            "clocks": dict(clocks, soak_steps_before_timing=soak_steps),
             "cpu_baseline": cpu,
         }
-        if ci is not None:
+        if R.ci is not None:
             line["config"]["attention"] = "cascade: each shared prefix read once per group"
         print(json.dumps(line), flush=True)
     if dist is not None:

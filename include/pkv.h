@@ -166,6 +166,44 @@ pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
                                       void *stream);
 
 /*
+ * pkv_paged_attention_varlen_range -- the same attention over a range of
+ * each request's keys, for work split along the sequence: sequence
+ * parallelism, where each GPU holds part of a long context, or any caller
+ * that attends to a context in pieces. ([page 1] §07: long-context chunked
+ * prefill, Flash-Decoding and sequence parallelism all split the sequence
+ * dimension and combine the pieces exactly by log-sum-exp renormalisation;
+ * pkv_lse_merge does that combination.)
+ *
+ * Arguments as pkv_paged_attention_varlen, plus two device arrays:
+ *   key_start_pos   [num_seqs] int32 >= 0: absolute position of the first
+ *                   key of request i's block table; its seq_lens[i] >= 1
+ *                   keys sit at key_start_pos[i] + p, p < seq_lens[i]
+ *   query_start_pos [num_seqs] int32 >= 0: absolute position of request i's
+ *                   first query; query j sits at query_start_pos[i] + j
+ * Query j of request i sees key p iff
+ *   key_start_pos[i] + p <= query_start_pos[i] + j     (causal, absolute)
+ * and the result is attention over exactly those keys: the normalised
+ * output and the natural-log lse of that key range. A query that sees no key
+ * of the range gets out = 0 and lse = -inf (an empty piece, which
+ * pkv_lse_merge ignores). The ordinary call is key_start_pos = 0 and
+ * query_start_pos = seq_len - query_len. seq_lens may be smaller than the
+ * query count here; max_seq_len only bounds seq_lens (>= 1).
+ * Merging the pieces of a context cut into ranges [s_r, e_r) with
+ * pkv_lse_merge gives the attention over the whole context (to rounding).
+ * Errors: as pkv_paged_attention_varlen; a NULL position array with
+ * num_tokens > 0 is PKV_ERR_INVALID_ARG; a negative position or a zero
+ * seq_len sets PKV_DEV_BAD_LENGTHS (that request is skipped).
+ */
+pkv_status pkv_paged_attention_varlen_range(
+    float *out, float *out_lse, const void *q, const void *kv_pool, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+    const int32_t *key_start_pos, const int32_t *query_start_pos, int32_t num_seqs,
+    int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+    int32_t partition_size, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+    void *stream);
+
+/*
  * pkv_lse_merge -- combine partial attention results by log-sum-exp
  * ([page 1] §07: chunked prefill, Flash-Decoding and sequence parallelism
  * renormalise their pieces with log-sum-exp).

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     library_path,
     lse_merge,
     paged_attention_varlen,
+    paged_attention_varlen_range,
 )
 
 __all__ = [
@@ -21,4 +22,5 @@ __all__ = [
     "library_path",
     "lse_merge",
     "paged_attention_varlen",
+    "paged_attention_varlen_range",
 ]

@@ -32,6 +32,9 @@ _SIGNATURES = {
     "pkv_paged_attention_varlen": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
+    "pkv_paged_attention_varlen_range": (
+        _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp] + [_i32] * 9
+        + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
     "pkv_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
     "pkv_paged_attention_varlen_noalloc": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
@@ -196,6 +199,59 @@ def paged_attention_varlen(q: torch.Tensor, kv_pool: torch.Tensor, block_table: 
         int(max_seq_len), h, hkv, d, bs, nb, float(scale), int(partition_size),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, q.device))
     _check(st, "paged_attention_varlen")
+    return out, out_lse
+
+
+def paged_attention_varlen_range(q: torch.Tensor, kv_pool: torch.Tensor,
+                                 block_table: torch.Tensor, cu_seqlens: torch.Tensor,
+                                 seq_lens: torch.Tensor, key_start_pos: torch.Tensor,
+                                 query_start_pos: torch.Tensor, max_query_len: int,
+                                 max_seq_len: int, *, out: torch.Tensor | None = None,
+                                 out_lse: torch.Tensor | None = None, scale: float | None = None,
+                                 partition_size: int = -1, workspace: torch.Tensor | None = None,
+                                 dev_status: torch.Tensor | None = None, stream=None):
+    """Attention over a range of each request's keys (``pkv_paged_attention_varlen_range``).
+
+    Request i's table holds ``seq_lens[i]`` keys at absolute positions
+    ``key_start_pos[i] + p``; its queries sit at ``query_start_pos[i] + j``
+    and see the keys at or before their own position. Returns the normalised
+    piece ``(out, out_lse)``; pieces of one context merge with :func:`lse_merge`.
+    """
+    _need(q, torch.bfloat16, 3, "q")
+    _need(kv_pool, torch.bfloat16, 5, "kv_pool")
+    _need(block_table, torch.int32, 2, "block_table")
+    for t, name in ((cu_seqlens, "cu_seqlens"), (seq_lens, "seq_lens"),
+                    (key_start_pos, "key_start_pos"), (query_start_pos, "query_start_pos")):
+        _need(t, torch.int32, 1, name)
+    t, h, d = q.shape
+    _, nb, bs, hkv, d2 = kv_pool.shape
+    if d2 != d:
+        raise ValueError("q and kv_pool head_dim differ")
+    b = seq_lens.shape[0]
+    if (cu_seqlens.shape[0] != b + 1 or block_table.shape[0] != b
+            or key_start_pos.shape[0] != b or query_start_pos.shape[0] != b):
+        raise ValueError("cu_seqlens must be [B+1]; block_table, key_start_pos and "
+                         "query_start_pos one row per request")
+    if out is None:
+        out = torch.empty((t, h, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, 3, "out")
+    if out_lse is not None:
+        _need(out_lse, torch.float32, 2, "out_lse")
+    if dev_status is not None:
+        _need(dev_status, torch.int32, 1, "dev_status")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attention_workspace_size(b, t, h, hkv, d, max_seq_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().pkv_paged_attention_varlen_range(
+        _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), _ptr(block_table),
+        block_table.shape[1], _ptr(cu_seqlens), _ptr(seq_lens), _ptr(key_start_pos),
+        _ptr(query_start_pos), b, t, int(max_query_len), int(max_seq_len), h, hkv, d, bs, nb,
+        float(scale), int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status),
+        _stream(stream, q.device))
+    _check(st, "paged_attention_varlen_range")
     return out, out_lse
 
 

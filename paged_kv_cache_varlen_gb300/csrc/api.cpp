@@ -2,8 +2,10 @@
 // argument validation, TMA tensor-map encoding and kernel dispatch.
 //
 // Nothing here allocates device memory, synchronises a stream or keeps
-// state across calls (the only cached item is the driver entry point of
-// cuTensorMapEncodeTiled and per-kernel shared-memory attributes).
+// state across calls (the only cached items are the driver entry point of
+// cuTensorMapEncodeTiled and, per device, the kernels' shared-memory limits).
+// Every host-side check and tensor-map encoding of a call happens before its
+// first launch, so a rejected call enqueues nothing.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -157,17 +159,172 @@ CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_g
   return c;
 }
 
+
+// One attention call after every host-side check, with its tensor maps
+// encoded: nothing has been enqueued yet. `empty` marks a call with no
+// tokens (a no-op).
+struct AttnPlan {
+  AttnParams p{};
+  CUtensorMap kv_rows{};  // decode: 16-key boxes of whole rows of one KV head
+  CUtensorMap q_map{};    // prefill: {64, G, 128/G} boxes of q
+  bool prefill = false;   // some request may have more queries than the decode kernel takes
+  bool empty = false;
+  WorkspaceLayout wl{};
+};
+
+pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q,
+                          const void* kv_pool, const int32_t* block_table,
+                          int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                          const int32_t* seq_lens, int32_t num_seqs, int32_t num_tokens,
+                          int32_t max_query_len, int32_t max_seq_len, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float scale, int32_t partition_size,
+                          const int32_t* key_start, const int32_t* query_start,
+                          int32_t* dev_status) {
+  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    a->empty = true;
+    return PKV_OK;
+  }
+  if (num_seqs == 0) return PKV_ERR_INVALID_ARG;
+  if (!out || !q || !kv_pool || !block_table || !cu_seqlens_q || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  // a key range may hold fewer keys than the request has queries
+  if (max_query_len < 1 || max_seq_len < (key_start ? 1 : max_query_len))
+    return PKV_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 || block_size > 256) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)2 * num_blocks * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int32_t group = num_heads / num_kv_heads;
+  if (max_query_len > 1 && (group > 128 || (128 % group) != 0)) return PKV_ERR_UNSUPPORTED;
+
+  int32_t ps = 0, np = 1;
+  if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
+  a->wl = workspace_layout(num_seqs, num_heads, head_dim, np);
+
+  AttnParams& p = a->p;
+  p.out = out;
+  p.out_lse = out_lse;
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv_pool = kv_pool;
+  p.block_table = block_table;
+  p.cu_seqlens = cu_seqlens_q;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.max_query_len = max_query_len;
+  p.max_seq_len = max_seq_len;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.part_size = ps;
+  p.num_parts = np;
+  p.ws_out = nullptr;
+  p.ws_lse = nullptr;
+  p.sched = nullptr;
+  p.status = dev_status;
+  p.key_start = key_start;
+  p.query_start = query_start;
+  // the decode kernel takes requests of up to 32 (query, head) rows: two
+  // subgroups of its 16-row MMA tiles
+  p.decode_max_q = 32 / group > 1 ? 32 / group : 1;
+  p.decode_max_rows = (max_query_len < p.decode_max_q ? max_query_len : p.decode_max_q) * group;
+  p.prefix_mode = 0;
+  p.kv_splits = 1;
+  p.split_out_stride = 0;
+  p.split_lse_stride = 0;
+
+  a->prefill = max_query_len > p.decode_max_q;
+  return PKV_OK;
+}
+
+// Encode the plan's TMA tensor maps (needs the driver; still enqueues nothing).
+pkv_status encode_plan(AttnPlan* a) {
+  const AttnParams& p = a->p;
+  const uint64_t D = (uint64_t)p.head_dim;
+  const uint64_t pool_rows = (uint64_t)2 * p.num_blocks * p.block_size;
+  // decode: a 16-key box of whole rows of one KV head, the pool viewed as
+  // [D/64][Hkv][rows][64] (strides 128 B, D*2, Hkv*D*2) so that the box
+  // lands as the 16 keys' first 128-byte halves, then their second halves:
+  // with the 128-byte swizzle, 8 consecutive keys of one half then sit in 8
+  // different bank groups (conflict-free ldmatrix)
+  const uint64_t dims[4] = {64, pool_rows, (uint64_t)p.num_kv_heads, D / 64};
+  const uint64_t strides[3] = {(uint64_t)p.num_kv_heads * D * 2, D * 2, 128};
+  const uint32_t box[4] = {64, 16, 1, (uint32_t)(D / 64)};
+  if (!encode_4d(&a->kv_rows, p.kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return PKV_ERR_CUDA;
+  const int32_t group = p.num_heads / p.num_kv_heads;
+  if (a->prefill &&
+      !encode_3d(&a->q_map, p.q, D, p.num_heads, p.num_tokens, D * 2,
+                 (uint64_t)p.num_heads * D * 2, 64, (uint32_t)group, (uint32_t)(128 / group),
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+// Point the plan at a caller's workspace after checking its size and alignment.
+pkv_status bind_workspace(AttnPlan* a, void* workspace, size_t workspace_bytes) {
+  if (!workspace || workspace_bytes < a->wl.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PKV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  a->p.sched = reinterpret_cast<int32_t*>(ws + a->wl.sched_off);
+  if (a->p.num_parts > 1) {
+    a->p.ws_out = reinterpret_cast<float*>(ws);
+    a->p.ws_lse = reinterpret_cast<float*>(ws + a->wl.lse_off);
+  }
+  return PKV_OK;
+}
+
+// Enqueue a planned call: the decode grid (and its split-KV merge grid), then
+// the prefill grid when some request is longer than the decode kernel takes.
+pkv_status launch_plan(const AttnPlan& a, cudaStream_t st) {
+  if (pkv::launch_decode_mma(a.p, a.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (a.prefill && pkv::launch_prefill(a.p, a.q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
-size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_seq_len,
-                                   int32_t partition_size) {
-  int32_t ps = 0, np = 1;
-  if (num_seqs <= 0 || num_heads <= 0 || !resolve_partition(max_seq_len, partition_size, &ps, &np))
-    return 0;
-  const WorkspaceLayout w = workspace_layout(num_seqs, num_heads, 1, np);
-  return w.total - w.sched_off;
+pkv_status attention_with_scratch(float* out, float* out_lse, const void* q, const void* kv_pool,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq,
+                                  const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                                  int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float scale, int32_t partition_size, int32_t* dev_status,
+                                  void* stream, size_t scratch_bytes,
+                                  cudaError_t (*scratch)(void**)) {
+  AttnPlan a;
+  pkv_status s = plan_attention(&a, out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
+                                cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, partition_size, nullptr, nullptr, dev_status);
+  if (s != PKV_OK || a.empty) return s;
+  if (a.wl.total > scratch_bytes) return PKV_ERR_WORKSPACE;
+  if ((s = encode_plan(&a)) != PKV_OK) return s;
+  void* base = nullptr;
+  if (scratch(&base) != cudaSuccess) return PKV_ERR_CUDA;
+  if ((s = bind_workspace(&a, base, scratch_bytes)) != PKV_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the work tickets must start at zero (an interrupted earlier call may
+  // have left them otherwise)
+  if (cudaMemsetAsync(a.p.sched, 0, kSchedBytes, st) != cudaSuccess) return PKV_ERR_CUDA;
+  return launch_plan(a, st);
 }
+
 }  // namespace pkv
 
 extern "C" {
@@ -230,95 +387,36 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
                                       int32_t num_blocks, float scale, int32_t partition_size,
                                       void* workspace, size_t workspace_bytes,
                                       int32_t* dev_status, void* stream) {
-  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_INVALID_ARG;
-  if (num_tokens == 0) return PKV_OK;
-  if (num_seqs == 0) return PKV_ERR_INVALID_ARG;
-  if (!out || !q || !kv_pool || !block_table || !cu_seqlens_q || !seq_lens)
-    return PKV_ERR_INVALID_ARG;
-  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
-    return PKV_ERR_INVALID_ARG;
-  if (block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || head_dim <= 0)
-    return PKV_ERR_INVALID_ARG;
-  if (max_query_len < 1 || max_seq_len < max_query_len) return PKV_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size % 16 != 0 || block_size > 256) return PKV_ERR_UNSUPPORTED;
-  if ((int64_t)2 * num_blocks * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  const int32_t group = num_heads / num_kv_heads;
-  if (max_query_len > 1 && (group > 128 || (128 % group) != 0)) return PKV_ERR_UNSUPPORTED;
+  AttnPlan a;
+  pkv_status s = plan_attention(&a, out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
+                                cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, partition_size, nullptr, nullptr, dev_status);
+  if (s != PKV_OK || a.empty) return s;
+  if ((s = bind_workspace(&a, workspace, workspace_bytes)) != PKV_OK) return s;
+  if ((s = encode_plan(&a)) != PKV_OK) return s;
+  return launch_plan(a, static_cast<cudaStream_t>(stream));
+}
 
-  int32_t ps = 0, np = 1;
-  if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
-  const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, np);
-  const size_t need = wl.total;
-  if (!workspace || workspace_bytes < need ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return PKV_ERR_WORKSPACE;
-
-  AttnParams p;
-  p.out = out;
-  p.out_lse = out_lse;
-  p.q = static_cast<const uint16_t*>(q);
-  p.kv_pool = kv_pool;
-  p.block_table = block_table;
-  p.cu_seqlens = cu_seqlens_q;
-  p.seq_lens = seq_lens;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_seqs = num_seqs;
-  p.num_tokens = num_tokens;
-  p.max_query_len = max_query_len;
-  p.max_seq_len = max_seq_len;
-  p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.head_dim = head_dim;
-  p.block_size = block_size;
-  p.num_blocks = num_blocks;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.part_size = ps;
-  p.num_parts = np;
-  p.ws_out = nullptr;
-  p.ws_lse = nullptr;
-  p.sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.sched_off);
-  // the decode kernel takes requests of up to 32 (query, head) rows: two
-  // subgroups of its 16-row MMA tiles
-  p.decode_max_q = 32 / group > 1 ? 32 / group : 1;
-  p.decode_max_rows = (max_query_len < p.decode_max_q ? max_query_len : p.decode_max_q) * group;
-  p.prefix_mode = 0;
-  p.kv_splits = 1;
-  p.split_out_stride = 0;
-  p.split_lse_stride = 0;
-  if (np > 1) {
-    p.ws_out = static_cast<float*>(workspace);
-    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_off);
-  }
-  p.status = dev_status;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  const uint64_t D = (uint64_t)head_dim;
-  const uint64_t pool_rows = (uint64_t)2 * num_blocks * block_size;
-  // decode: a 16-key box of whole rows of one KV head, the pool viewed as
-  // [D/64][Hkv][rows][64] (strides 128 B, D*2, Hkv*D*2) so that the box
-  // lands as the 16 keys' first 128-byte halves, then their second halves:
-  // with the 128-byte swizzle, 8 consecutive keys of one half then sit in 8
-  // different bank groups (conflict-free ldmatrix)
-  CUtensorMap kv_rows;
-  const uint64_t dims[4] = {64, pool_rows, (uint64_t)num_kv_heads, D / 64};
-  const uint64_t strides[3] = {(uint64_t)num_kv_heads * D * 2, D * 2, 128};
-  const uint32_t box[4] = {64, 16, 1, (uint32_t)(D / 64)};
-  if (!encode_4d(&kv_rows, kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-    return PKV_ERR_CUDA;
-  if (pkv::launch_decode_mma(p, kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
-
-  if (max_query_len > p.decode_max_q) {
-    CUtensorMap q_map;
-    if (!encode_3d(&q_map, q, D, num_heads, num_tokens, D * 2, (uint64_t)num_heads * D * 2, 64,
-                   (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
-      return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
-  }
-  return PKV_OK;
+pkv_status pkv_paged_attention_varlen_range(
+    float* out, float* out_lse, const void* q, const void* kv_pool, const int32_t* block_table,
+    int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+    const int32_t* key_start_pos, const int32_t* query_start_pos, int32_t num_seqs,
+    int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+    int32_t partition_size, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+    void* stream) {
+  if (num_tokens > 0 && (!key_start_pos || !query_start_pos)) return PKV_ERR_INVALID_ARG;
+  AttnPlan a;
+  pkv_status s = plan_attention(&a, out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
+                                cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, partition_size, key_start_pos,
+                                query_start_pos, dev_status);
+  if (s != PKV_OK || a.empty) return s;
+  if ((s = bind_workspace(&a, workspace, workspace_bytes)) != PKV_OK) return s;
+  if ((s = encode_plan(&a)) != PKV_OK) return s;
+  return launch_plan(a, static_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_copy_blocks(void* kv_pool, const int32_t* copy_src, const int32_t* copy_dst,
@@ -387,26 +485,26 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
   const int64_t bh = (int64_t)num_seqs * num_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // 1. empty prefix partials, one query per request for the tail pass
-  if (pkv::launch_cascade_prepare(part_lse, (int64_t)c.splits * bh, tail_cu, num_seqs, st) !=
-      cudaSuccess)
-    return PKV_ERR_CUDA;
-  // 2. tails: ordinary decode over each request's private blocks
-  pkv_status s = pkv_paged_attention_varlen(
-      part_out + (int64_t)c.splits * bh * head_dim, part_lse + (int64_t)c.splits * bh, q, kv_pool,
-      tail_tables, max_tail_blocks, tail_cu, tail_lens, num_seqs, num_seqs, 1, max_tail_len,
-      num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, -1,
-      ws + c.ws_off, c.ws_bytes, dev_status, stream);
+  // Every check and tensor-map encoding happens before the first launch.
+  // Tails: ordinary decode over each request's private blocks, one query per
+  // request (the cu_seqlens the preparation kernel writes).
+  AttnPlan tails;
+  pkv_status s = plan_attention(
+      &tails, part_out + (int64_t)c.splits * bh * head_dim, part_lse + (int64_t)c.splits * bh, q,
+      kv_pool, tail_tables, max_tail_blocks, tail_cu, tail_lens, num_seqs, num_seqs, 1,
+      max_tail_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, -1, nullptr,
+      nullptr, dev_status);
   if (s != PKV_OK) return s;
-  // 3. prefixes: every group's queries against its shared blocks, once, on
-  //    the tensor cores (the prefill kernel in prefix mode), cut into key
-  //    segments
-  if (num_prefix_groups > 0 && max_prefix_len > 0) {
-    AttnParams p;
+  if ((s = bind_workspace(&tails, ws + c.ws_off, c.ws_bytes)) != PKV_OK) return s;
+  if ((s = encode_plan(&tails)) != PKV_OK) return s;
+  // Prefixes: every group's queries against its shared blocks, once, on the
+  // tensor cores (the prefill kernel in prefix mode), cut into key segments.
+  const bool prefixes = num_prefix_groups > 0 && max_prefix_len > 0;
+  AttnParams p = tails.p;
+  CUtensorMap q_map{};
+  if (prefixes) {
     p.out = part_out;
     p.out_lse = part_lse;
-    p.q = static_cast<const uint16_t*>(q);
-    p.kv_pool = kv_pool;
     p.block_table = prefix_tables;
     p.cu_seqlens = group_starts;
     p.seq_lens = prefix_lens;
@@ -415,18 +513,11 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.num_tokens = num_seqs;
     p.max_query_len = max_group_size;
     p.max_seq_len = max_prefix_len;
-    p.num_heads = num_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.head_dim = head_dim;
-    p.block_size = block_size;
-    p.num_blocks = num_blocks;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.part_size = 0;
     p.num_parts = 1;
     p.ws_out = nullptr;
     p.ws_lse = nullptr;
-      p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
-    p.status = dev_status;
+    p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
     p.decode_max_q = 0;  // the prefix pass takes every group
     p.decode_max_rows = 0;
     p.prefix_mode = 1;
@@ -434,12 +525,19 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.split_out_stride = bh * head_dim;
     p.split_lse_stride = bh;
     const uint64_t D = (uint64_t)head_dim;
-    CUtensorMap q_map;
     if (!encode_3d(&q_map, q, D, num_heads, num_seqs, D * 2, (uint64_t)num_heads * D * 2, 64,
                    (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
       return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
   }
+
+  // 1. empty prefix partials, one query per request for the tail pass
+  if (pkv::launch_cascade_prepare(part_lse, (int64_t)c.splits * bh, tail_cu, num_seqs, st) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  // 2. tails
+  if ((s = launch_plan(tails, st)) != PKV_OK) return s;
+  // 3. prefixes
+  if (prefixes && pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
   // 4. merge every request's prefix segments and tail by log-sum-exp
   return pkv::launch_lse_merge(out, out_lse, part_out, part_lse, c.splits + 1, bh, head_dim, st) ==
                  cudaSuccess

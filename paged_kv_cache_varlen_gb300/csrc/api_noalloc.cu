@@ -58,25 +58,13 @@ extern "C" pkv_status pkv_paged_attention_varlen_noalloc(
     int32_t num_seqs, int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
     int32_t num_blocks, float scale, int32_t partition_size, int32_t* dev_status, void* stream) {
-  // The scratch this call needs is what pkv_paged_attention_varlen would ask for.
-  const size_t need = pkv_attention_workspace_size(num_seqs, num_tokens, num_heads, num_kv_heads,
-                                                   head_dim, max_seq_len, partition_size);
-  if (need > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;  // beyond the built-in scratch
-  void* scratch = nullptr;
-  if (need > 0) {
-    if (noalloc_scratch(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
-    // The prefill work tickets (the last piece of the scratch) must start
-    // at zero. Calls leave them zero, but an
-    // interrupted call may not, so clear them every time.
-    const size_t cnt_bytes =
-        pkv::attention_zeroed_tail_bytes(num_seqs, num_heads, max_seq_len, partition_size);
-    if (cudaMemsetAsync(static_cast<char*>(scratch) + (need - cnt_bytes), 0, cnt_bytes,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
-  return pkv_paged_attention_varlen(out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
-                                    cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
-                                    max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
-                                    num_blocks, scale, partition_size, scratch, need, dev_status,
-                                    stream);
+  // Every argument is checked before the scratch is looked up or touched;
+  // then the call needs at most the built-in scratch (what
+  // pkv_attention_workspace_size gives for these sizes), whose work tickets
+  // are cleared on the stream before the kernels run.
+  return pkv::attention_with_scratch(out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
+                                     cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
+                                     max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                                     num_blocks, scale, partition_size, dev_status, stream,
+                                     kNoAllocScratchBytes, noalloc_scratch);
 }

@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int32_t t0 = __ldg(p.cu_seqlens + i);
   const int32_t t1 = __ldg(p.cu_seqlens + i + 1);
   const int32_t L = __ldg(p.seq_lens + i);
+  const bool ranged = p.key_start != nullptr;
+  const int32_t kstart = ranged ? __ldg(p.key_start + i) : 0;
+  const int32_t qstart = ranged ? __ldg(p.query_start + i) : 0;
   // several queries (a verification step) take partition 0 only, kbeg = 0
   const int32_t kbeg = part * p.part_size;
   const int32_t* bt = p.block_table + (int64_t)i * p.max_blocks;
@@ -151,10 +154,16 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int row0 = sub * kRows;
   if (row0 >= qlen * group) return;  // no row of this request in the subgroup
   const int rows = min(kRows, qlen * group - row0);  // rows of this CTA
-  if (L < qlen || L > p.max_seq_len || L > p.max_blocks * p.block_size) {
+  if ((ranged ? (L < 1 || kstart < 0 || qstart < 0) : L < qlen) || L > p.max_seq_len ||
+      L > p.max_blocks * p.block_size) {
     if (leader) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return;
   }
+  // position of the request's first query among its keys (query j sees keys
+  // 0 .. qpos0 + j); a key range may start after a query, which then sees
+  // nothing of it
+  const int32_t qpos0 =
+      ranged ? (int32_t)max(-(1 << 30), min(1 << 30, qstart - kstart)) : L - qlen;
   // several queries: one partition over every key, with the causal limit per
   // row; one query: the split-KV partitions
   if (qlen > 1 && part > 0) return;
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   auto row_token = [&](int rr) { return t0 + (row0 + rr) / group; };
   auto row_head = [&](int rr) { return kvh * group + (row0 + rr) % group; };
   auto row_limit = [&](int rr) {  // keys < limit are visible to the row
-    return rr < rows ? min(kend, L - qlen + (row0 + rr) / group + 1) : 0;
+    return rr < rows ? min(kend, qpos0 + (row0 + rr) / group + 1) : 0;
   };
   uint32_t qa[KS][4];
   {
@@ -539,13 +548,10 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   constexpr size_t SLOT = 2 * kChunk * D * 2;
   const size_t smem = 1024 + kWarps * SPW * SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
   auto kernel = decode_mma_kernel<D, SPW, MINB>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit limit;
+  if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), (int)smem);
+      e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_kv_heads * ((p.decode_max_rows + kRows - 1) / kRows), p.num_parts,
                      p.num_seqs);

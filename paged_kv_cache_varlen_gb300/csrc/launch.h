@@ -6,7 +6,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace pkv {
+
+// A kernel's dynamic shared-memory limit is a per-device attribute: raise it
+// once on every device the process launches the kernel on (thread-safe; a
+// process may drive several GPUs from several host threads).
+class SmemLimit {
+ public:
+  cudaError_t ensure(const void* func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 struct KvWriteParams {
   void* pool;                 // [2][NB][BS][Hkv][D] bf16
@@ -40,6 +67,11 @@ struct AttnParams {
   int32_t* sched;             // prefill work tickets: [0] next item, [1] CTAs done;
                               // zero between calls
   int32_t* status;
+  // key-range mode (both null otherwise): the keys of request i in its block
+  // table sit at absolute positions key_start[i] + p, its queries at
+  // query_start[i] + j; query j sees key p iff key_start + p <= query_start + j
+  const int32_t* key_start;
+  const int32_t* query_start;
   // requests of 1 .. decode_max_q queries run on the decode kernel (its MMA
   // rows are (query, head) pairs, at most decode_max_rows per request in the
   // launch); longer ones on the prefill kernel
@@ -56,10 +88,20 @@ struct AttnParams {
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 
-// Bytes at the end of an attention workspace that must be zero before a call
-// (and that every completed call leaves zero): the prefill work tickets.
-size_t attention_zeroed_tail_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_seq_len,
-                                   int32_t partition_size);
+// pkv_paged_attention_varlen with its workspace in caller-independent scratch
+// of `scratch_bytes` bytes whose device address `scratch` returns (for the
+// current device). Every host-side check runs first; a call whose workspace
+// would exceed the scratch returns PKV_ERR_WORKSPACE; nothing is enqueued on
+// an error. The work tickets are cleared on the stream before the launches.
+int32_t attention_with_scratch(float* out, float* out_lse, const void* q, const void* kv_pool,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                               int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, int32_t partition_size, int32_t* dev_status,
+                               void* stream, size_t scratch_bytes,
+                               cudaError_t (*scratch)(void**));
 
 // Decode kernel (query_len == 1 requests): TMA-staged pages, QK^T and PV on
 // the warp-level tensor cores (mma.sync); split-KV partitions merged by a

@@ -125,6 +125,7 @@ struct Bars {
 
 struct PrefillItem {
   int req, kvh, j0, j1, t0, qlen, L, kv_end, n_tiles;
+  int qpos0;  // position of the request's first query among its keys
   int jb;   // first key tile of the item (a key segment in prefix mode)
   int seg;  // key segment (prefix mode), else 0
 };
@@ -162,7 +163,10 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP,
   }
   if (qlen <= p.decode_max_q) return 0;  // short requests run on the decode kernel
   const int32_t L = __ldg(p.seq_lens + r);
-  if (qlen > p.max_query_len || L < qlen || L > p.max_seq_len ||
+  const bool bad_range =
+      p.key_start ? (L < 1 || __ldg(p.key_start + r) < 0 || __ldg(p.query_start + r) < 0)
+                  : L < qlen;
+  if (qlen > p.max_query_len || bad_range || L > p.max_seq_len ||
       L > p.max_blocks * p.block_size) {
     if (flag) set_status(p.status, PKV_DEV_BAD_LENGTHS);
     return 0;
@@ -218,6 +222,7 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
   d.qlen = __ldg(p.cu_seqlens + lo + 1) - d.t0;
   d.L = __ldg(p.seq_lens + lo);
   const int ntq = (d.qlen + QP - 1) / QP;
+  d.qpos0 = d.L - d.qlen;
   if (p.prefix_mode) {
     const int segs = prefix_segment_count(d.L, p.kv_splits);
     const int tps = prefix_tiles_per_segment(d.L, p.kv_splits);
@@ -233,8 +238,14 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
   const int qt = ntq - 1 - (u - pref[lo]);  // later (heavier) units first
   d.j0 = qt * QP;
   d.j1 = min(d.qlen, d.j0 + QP);
-  d.kv_end = d.L - d.qlen + d.j1;  // keys [0, kv_end) are needed
-  d.n_tiles = (d.kv_end + kBN - 1) / kBN;
+  if (p.key_start) {  // key range: the queries' positions come from the caller
+    const int64_t rel = (int64_t)__ldg(p.query_start + lo) - __ldg(p.key_start + lo);
+    d.qpos0 = (int)max((int64_t)-(1 << 30), min((int64_t)(1 << 30), rel));
+  }
+  // keys [0, kv_end) are needed; at least one tile runs (fully masked when no
+  // key is visible) so that the item's rows are written
+  d.kv_end = max(0, min(d.L, d.qpos0 + d.j1));
+  d.n_tiles = max(1, (d.kv_end + kBN - 1) / kBN);
   d.jb = 0;
   d.seg = 0;
   return d;
@@ -563,7 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PrefillItem d = prefill_item(p, pref, QP, it);
       const int qj = d.j0 + x * QT + rq;
       const bool row_valid = qj < d.j1;
-      const int pos = (row_valid && !p.prefix_mode) ? (d.L - d.qlen + qj) : (d.kv_end - 1);
+      // the row's last visible key (a key range may end before the query)
+      const int pos =
+          (row_valid && !p.prefix_mode) ? min(d.qpos0 + qj, d.kv_end - 1) : (d.kv_end - 1);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < d.n_tiles; ++j) {
         const int gg = gt + j;
@@ -741,13 +754,10 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cuda
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kernel = prefill_kernel<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit limit;
+  if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), 227 * 1024);
+      e != cudaSuccess)
+    return e;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

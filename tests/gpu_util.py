@@ -60,19 +60,26 @@ class DeviceStep:
         return int(self.status.item())
 
 
-def sample_rows(w: wl.Workload, per_chunk: int = 32, seed: int = 0) -> np.ndarray:
-    """Every decode token, plus `per_chunk` rows of each longer request
-    (always its first and last query, the rest seeded at random)."""
-    rng = np.random.default_rng(seed)
-    rows = []
-    for i in range(w.num_seqs):
-        a, b = int(w.cu_seqlens[i]), int(w.cu_seqlens[i + 1])
-        if b - a <= per_chunk:
-            rows.extend(range(a, b))
-        else:
-            pick = set(rng.choice(np.arange(a + 1, b - 1), per_chunk - 2, replace=False).tolist())
-            rows.extend(sorted(pick | {a, b - 1}))
-    return np.array(rows, dtype=np.int32)
+def guarded(shape, dtype, guard: int = 8192, device="cuda"):
+    """A tensor of `shape` inside a larger buffer whose `guard` elements on
+    each side hold a sentinel bit pattern (stands in for a memory checker:
+    a kernel that writes outside the tensor changes a sentinel). Returns
+    (buffer, view); the view starts guard * itemsize bytes in (a multiple of
+    256 for every dtype here)."""
+    n = 1
+    for d in shape:
+        n *= d
+    bits = {torch.float32: (torch.int32, 0x7FBADBAD), torch.bfloat16: (torch.int16, 0x7DAD),
+            torch.int32: (torch.int32, 0x5EA1ED), torch.uint8: (torch.uint8, 0xA5)}[dtype]
+    buf = torch.full((guard + n + guard,), bits[1], dtype=bits[0], device=device)
+    view = buf.view(dtype)[guard:guard + n].view(shape)
+    return buf, view
+
+
+def guards_intact(buf: torch.Tensor, n: int, guard: int = 8192) -> bool:
+    """True when both sentinel bands of a `guarded` buffer are unchanged."""
+    sentinel = buf[0].item()
+    return bool(torch.all(buf[:guard] == sentinel) and torch.all(buf[guard + n:] == sentinel))
 
 
 def compare(out: torch.Tensor, lse: torch.Tensor, ref_out: np.ndarray, ref_lse: np.ndarray,

@@ -166,3 +166,88 @@ def test_cascade_workspace_size_arithmetic(lib):
 ])
 def test_copy_blocks_rejects_before_launch(lib, args, status):
     assert lib.pkv_copy_blocks(*args) == status
+
+
+# On a host without a GPU, the first CUDA step of a call that passed every
+# host-side check fails with PKV_ERR_CUDA (3). A rejection status other than 3
+# therefore shows that the call stopped before touching CUDA, i.e. before it
+# could enqueue anything.
+
+def _cascade(lib, **over):
+    args = dict(out=256, out_lse=None, q=256, kv_pool=256, num_prefix_groups=1,
+                group_starts=256, prefix_lens=256, prefix_tables=256, max_prefix_blocks=4,
+                max_group_size=8, max_prefix_len=64, tail_tables=256, max_tail_blocks=4,
+                tail_lens=256, max_tail_len=64, num_seqs=8, num_heads=32, num_kv_heads=8,
+                head_dim=128, block_size=16, num_blocks=64, scale=0.088, workspace=256,
+                workspace_bytes=1 << 30, dev_status=None, stream=None)
+    args.update(over)
+    return lib.pkv_cascade_decode(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"head_dim": 96}, 2),            # rejected before the preparation kernel is launched
+    ({"block_size": 8}, 2),
+    ({"out": None}, 1),
+    ({"workspace_bytes": 1024}, 4),
+    ({}, 3),                          # every check passes: the first CUDA step fails here
+])
+def test_cascade_rejects_before_any_launch(lib, over, status):
+    assert _cascade(lib, **over) == status
+
+
+def _noalloc(lib, **over):
+    args = dict(out=256, out_lse=None, q=256, kv_pool=256, block_table=256, max_blocks=512,
+                cu=256, seq_lens=256, num_seqs=1, num_tokens=1, max_query_len=1,
+                max_seq_len=8192, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                num_blocks=1024, scale=0.088, partition_size=-1, dev_status=None, stream=None)
+    args.update(over)
+    return lib.pkv_paged_attention_varlen_noalloc(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"out": None}, 1),
+    ({"q": None}, 1),
+    ({"head_dim": 96}, 2),
+    ({"num_tokens": 0, "out": None}, 0),   # an empty batch touches nothing
+    # bad arguments are reported as such even when the sizes are beyond the scratch
+    ({"out": None, "num_seqs": 4096, "num_tokens": 4096}, 1),
+])
+def test_noalloc_checks_arguments_before_its_scratch(lib, over, status):
+    assert _noalloc(lib, **over) == status
+
+
+def test_noalloc_scratch_boundary(lib):
+    """16 MiB of built-in scratch: at 32 heads, D = 128 and 8 automatic
+    1024-token partitions a request needs 8 * 32 * (128 + 1) * 4 bytes of
+    partials, so 127 requests fit and 128 do not."""
+    per_req = 8 * 32 * 128 * 4 + 8 * 32 * 4
+    assert lib.pkv_attention_workspace_size(127, 127, 32, 8, 128, 8192, -1) == \
+        127 * per_req + 256 <= 16 << 20
+    assert lib.pkv_attention_workspace_size(128, 128, 32, 8, 128, 8192, -1) > 16 << 20
+    # 127 passes the size check (and then fails at the first CUDA step on a
+    # host without a GPU); 128 is rejected by it
+    assert _noalloc(lib, num_seqs=127, num_tokens=127) == 3
+    assert _noalloc(lib, num_seqs=128, num_tokens=128) == 4
+
+
+def _range(lib, **over):
+    args = dict(out=256, out_lse=None, q=256, kv_pool=256, block_table=256, max_blocks=4,
+                cu=256, seq_lens=256, key_start=256, query_start=256, num_seqs=1, num_tokens=4,
+                max_query_len=4, max_seq_len=2, num_heads=32, num_kv_heads=8, head_dim=128,
+                block_size=16, num_blocks=8, scale=0.088, partition_size=-1, workspace=256,
+                workspace_bytes=1 << 20, dev_status=None, stream=None)
+    args.update(over)
+    return lib.pkv_paged_attention_varlen_range(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"key_start": None}, 1),
+    ({"query_start": None}, 1),
+    ({"max_seq_len": 0}, 1),
+    ({"head_dim": 96}, 2),
+    ({"workspace": None}, 4),
+    ({"num_tokens": 0, "key_start": None}, 0),
+    ({}, 3),          # a range may hold fewer keys than queries: accepted
+])
+def test_range_rejects_before_launch(lib, over, status):
+    assert _range(lib, **over) == status
