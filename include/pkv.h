@@ -65,6 +65,10 @@ typedef int32_t pkv_status;
                                        max_blocks_per_seq * block_size */
 #define PKV_DEV_TIMEOUT 8           /* an internal pipeline wait gave up; outputs of the
                                        affected tile are unspecified */
+#define PKV_DEV_V_RANGE 16          /* the chunked-prefill kernel met a V value of magnitude
+                                       >= 65536 (or inf / NaN), beyond the fp16 range its
+                                       P.V product uses; that request's outputs are
+                                       unspecified */
 
 /*
  * pkv_kv_cache_write -- scatter the step's new K/V rows into the paged pool.

@@ -64,6 +64,7 @@ DEV_BAD_SLOT = 1
 DEV_BAD_BLOCK = 2
 DEV_BAD_LENGTHS = 4
 DEV_TIMEOUT = 8
+DEV_V_RANGE = 16
 
 
 class PkvError(RuntimeError):

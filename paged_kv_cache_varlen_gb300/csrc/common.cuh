@@ -240,6 +240,11 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(uint32_t M, uint32_t N, b
          | ((M >> 4) << 24);       // M / 16
 }
 
+// The same descriptor with fp16 A and B (fp32 D).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return umma_idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10));
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes
 // with CU_TENSOR_MAP_SWIZZLE_128B into 1024-byte aligned buffers).
 //   K-major operand: rows of 128 bytes (64 bf16 along K), 8-row groups of
@@ -281,6 +286,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),       \
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),       \
       "r"(r[29]), "r"(r[30]), "r"(r[31])                                                         \
+      : "memory")
+
+#define PKV_TMEM_ST16(taddr, r)                                                                  \
+  asm volatile(                                                                                  \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"    \
+      "%13,%14,%15,%16};" ::"r"(taddr),                                                          \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),         \
+      "r"(r[15])                                                                                 \
       : "memory")
 
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -68,18 +68,42 @@ constexpr int kQT = 2;                               // Q tiles per work item
 constexpr int kBN = 128;                             // keys per KV tile
 constexpr int kNS = 2;                               // stages of each of the K and V rings
 constexpr int kSub = 16;                             // keys per gathered sub-block
-constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 4*kQT-1
-constexpr int kProducers = 64;                       // two K/V producer warps
-constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // first producer warp (also issues Q)
-constexpr int kMmaWarp = kProdWarp0 + kProducers / 32;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 7 (warpgroups 0, 1)
+constexpr int kProducers = 64;                       // threads of each producer role
+constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warps 8-9: K tiles (warp 8 also Q)
+constexpr int kVWarp0 = kProdWarp0 + kProducers / 32;  // warps 10-11: V tiles, to fp16
+constexpr int kMmaWarp = kVWarp0 + kProducers / 32;  // warp 12
+constexpr int kConvWarp0 = kMmaWarp + 1;             // warps 13-15: V to fp16 (fp16 P only)
+constexpr int kConverters = 3 * 32;
+constexpr int kThreads = 512;                        // four warpgroups
+// registers per thread: launched with 128; the softmax warpgroups take 152,
+// the producer / MMA warpgroups give theirs down to 104 (2*152 + 2*104 = 4*128)
+constexpr int kSoftmaxRegs = 152;
+constexpr int kOtherRegs = 104;
+static_assert(2 * kSoftmaxRegs + 2 * kOtherRegs == 4 * (65536 / kThreads),
+              "the register split adds up to the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRing = 4;  // work items announced ahead of the roles that consume them
-// readers of an announced item: the second producer warp, the MMA thread and
-// the eight softmax warps (one lane each)
-constexpr int kItemReaders = 1 + 1 + kSoftmaxThreads / 32;
+// readers of an announced item: producer warps 9-11, the MMA thread, the
+// eight softmax warps (one lane each) and, with fp16 P, the three converter warps
+__host__ __device__ constexpr int item_readers(bool f16p) {
+  return 3 + 1 + kSoftmaxThreads / 32 + (f16p ? 3 : 0);
+}
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
+
+// The work list handed out by the tickets. For batches of at most
+// kSortMax requests it holds the requests that have work, heaviest first
+// (by the key tiles of their heaviest unit): an approximate
+// longest-processing-time-first schedule, since a CTA takes the next ticket
+// when it finishes an item (in request order the longest prefill chunks came
+// last and left most SMs idle for their tail). Larger batches keep request
+// order. Shared-memory ints: key, candidate, order and prefix arrays of
+// B + 1 each when sorted, else the prefix array alone.
+constexpr int kSortMax = 2048;
+__host__ __device__ constexpr size_t work_list_ints(int num_seqs) {
+  return num_seqs <= kSortMax ? 4 * ((size_t)num_seqs + 1) : (size_t)num_seqs + 1;
+}
 
 template <int D>
 struct PrefillLayout {
@@ -90,17 +114,19 @@ struct PrefillLayout {
   static constexpr int K_OFF = Q_OFF + kQT * TILE_BYTES;   // [kNS] K tiles
   static constexpr int V_OFF = K_OFF + kNS * TILE_BYTES;   // [kNS] V tiles
   static constexpr int BAR_OFF = V_OFF + kNS * TILE_BYTES;
-  static constexpr int PREF_OFF = BAR_OFF + 512;
+  static constexpr int PREF_OFF = BAR_OFF + 512;   // the work list (see WorkList)
   // keep one CTA per SM (each CTA allocates all 512 TMEM columns)
   static size_t bytes(int num_seqs) {
-    const size_t need = 1024 + PREF_OFF + (size_t)(num_seqs + 1) * 4;
+    const size_t need = 1024 + PREF_OFF + work_list_ints(num_seqs) * 4;
     return need > 120 * 1024 ? need : 120 * 1024;
   }
   // TMEM columns: S of tile x (P written in place), then O of tile x
   __device__ static constexpr uint32_t s_col(int x) { return 128u * (uint32_t)x; }
   __device__ static constexpr uint32_t o_col(int x) { return 128u * (uint32_t)(kQT + x); }
-  // P of keys 16*kk .. 16*kk+15 inside an S buffer: each 32-key piece holds
-  // 16 columns of packed hi then 16 columns of packed lo
+  // P of keys 16*kk .. 16*kk+15 inside an S buffer. fp16 P: pairs in 8
+  // columns. bf16 P: each 32-key piece holds 16 columns of packed high parts
+  // then 16 columns of packed remainders.
+  __device__ static constexpr uint32_t p_col(int kk) { return 8u * (uint32_t)kk; }
   __device__ static constexpr uint32_t p_hi_col(int kk) {
     return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
   }
@@ -111,6 +137,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kNS], k_empty[kNS];
   uint64_t v_full[kNS], v_empty[kNS];
+  uint64_t v_landed[kNS];  // fp16 P: V copies arrived (bf16), not yet converted
   uint64_t s_full[kQT];   // QK^T of the tile landed in S_x
   uint64_t p_ready[kQT];  // the warpgroup stored P_x (and rescaled O_x)
   uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
@@ -174,59 +201,150 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP,
   return (qlen + QP - 1) / QP;
 }
 
-// pref[r] = work units of requests before r; pref[B] = total. All threads.
-__device__ __forceinline__ int prefill_prefix(const AttnParams& p, int* pref, int32_t* scan,
-                                              int QP) {
-  const int B = p.num_seqs;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool flag = blockIdx.x == 0;
-  const int per = (B + kThreads - 1) / kThreads;
-  const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
-  int sum = 0;
-  for (int r = r0; r < r1; ++r) sum += prefill_units(p, r, QP, flag);
-  int incl = sum;
+// Key tiles of request r's heaviest work unit (its last queries see the
+// most keys), for the heaviest-first order; call only for requests with work.
+__device__ __forceinline__ int prefill_weight(const AttnParams& p, int r) {
+  const int32_t L = __ldg(p.seq_lens + r);
+  if (p.prefix_mode) return prefix_tiles_per_segment(L, p.kv_splits);
+  const int32_t qlen = __ldg(p.cu_seqlens + r + 1) - __ldg(p.cu_seqlens + r);
+  int64_t end = L;  // ordinary call: the last query sees every key
+  if (p.key_start) {
+    end = (int64_t)__ldg(p.query_start + r) - __ldg(p.key_start + r) + qlen;
+    end = end < 0 ? 0 : (end > L ? L : end);
+  }
+  return (int)((end + kBN - 1) / kBN);
+}
+
+// Exclusive prefix sum of one value per thread over the CTA; *total gets the
+// sum. All threads; two __syncthreads.
+__device__ __forceinline__ int block_exclusive_scan(int v, int32_t* scan, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(kFullMask, incl, o);
-    if (lane >= o) incl += v;
+    const int t = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += t;
   }
   if (lane == 31) scan[warp] = incl;
   __syncthreads();
-  int base = 0;
-  for (int w = 0; w < warp; ++w) base += scan[w];
-  int run = base + incl - sum;
-  for (int r = r0; r < r1; ++r) {
-    pref[r] = run;
-    run += prefill_units(p, r, QP, false);
+  int base = 0, all = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) base += scan[w];
+    all += scan[w];
   }
-  if (tid == kThreads - 1) pref[B] = run;
   __syncthreads();
-  return pref[B];
+  *total = all;
+  return base + incl - v;
 }
 
-__device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const int* pref, int QP,
+// The work list in shared memory: positions 0 .. n-1 in the order their units
+// are handed out; request of position k = sorted ? order[k] : k; units
+// before position k = pref[k], pref[n] = total.
+struct WorkList {
+  const int* order;
+  const int* pref;
+  int n;
+  bool sorted;
+};
+
+// Builds the work list (all threads); returns it and sets *total_units.
+__device__ __forceinline__ WorkList prefill_work_list(const AttnParams& p, int* base,
+                                                      int32_t* scan, int QP, int* total_units) {
+  const int B = p.num_seqs;
+  const int tid = threadIdx.x;
+  const bool flag = blockIdx.x == 0;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+  WorkList wl;
+  if (B > kSortMax) {  // request order: pref over every request
+    int* pref = base;
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) sum += prefill_units(p, r, QP, flag);
+    int total = 0;
+    int run = block_exclusive_scan(sum, scan, &total);
+    for (int r = r0; r < r1; ++r) {
+      pref[r] = run;
+      run += prefill_units(p, r, QP, false);
+    }
+    if (tid == kThreads - 1) pref[B] = total;
+    __syncthreads();
+    *total_units = total;
+    wl.order = nullptr;
+    wl.pref = pref;
+    wl.n = B;
+    wl.sorted = false;
+    return wl;
+  }
+  int* key = base;               // [B] weight of each request with work, -1 otherwise
+  int* cand = base + (B + 1);    // [n] requests with work, in request order
+  int* order = cand + (B + 1);   // [n] the same, heaviest first
+  int* pref = order + (B + 1);   // [n + 1]
+  int cnt = 0;
+  for (int r = r0; r < r1; ++r) {
+    const bool work = prefill_units(p, r, QP, flag) > 0;
+    key[r] = work ? prefill_weight(p, r) : -1;
+    cnt += work ? 1 : 0;
+  }
+  int n = 0;
+  int pos = block_exclusive_scan(cnt, scan, &n);
+  for (int r = r0; r < r1; ++r)
+    if (key[r] >= 0) cand[pos++] = r;
+  __syncthreads();
+  // rank among the candidates: heavier first, ties by request index
+  for (int i = tid; i < n; i += kThreads) {
+    const int r = cand[i], k = key[r];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const int r2 = cand[j], k2 = key[r2];
+      rank += (k2 > k || (k2 == k && r2 < r)) ? 1 : 0;
+    }
+    order[rank] = r;
+  }
+  __syncthreads();
+  const int per2 = (n + kThreads - 1) / kThreads;
+  const int k0 = min(n, tid * per2), k1 = min(n, k0 + per2);
+  int sum = 0;
+  for (int k = k0; k < k1; ++k) sum += prefill_units(p, order[k], QP, false);
+  int total = 0;
+  int run = block_exclusive_scan(sum, scan, &total);
+  for (int k = k0; k < k1; ++k) {
+    pref[k] = run;
+    run += prefill_units(p, order[k], QP, false);
+  }
+  if (tid == kThreads - 1) pref[n] = total;
+  __syncthreads();
+  *total_units = total;
+  wl.order = order;
+  wl.pref = pref;
+  wl.n = n;
+  wl.sorted = true;
+  return wl;
+}
+
+__device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const WorkList& wl, int QP,
                                                     int it) {
   PrefillItem d;
   const int u = it / p.num_kv_heads;
   d.kvh = it - u * p.num_kv_heads;
-  int lo = 0, hi = p.num_seqs;  // largest lo with pref[lo] <= u
+  int lo = 0, hi = wl.n;  // largest lo with pref[lo] <= u
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (pref[mid] <= u)
+    if (wl.pref[mid] <= u)
       lo = mid;
     else
       hi = mid;
   }
-  d.req = lo;
-  d.t0 = __ldg(p.cu_seqlens + lo);
-  d.qlen = __ldg(p.cu_seqlens + lo + 1) - d.t0;
-  d.L = __ldg(p.seq_lens + lo);
+  const int req = wl.sorted ? wl.order[lo] : lo;
+  const int local = u - wl.pref[lo];
+  d.req = req;
+  d.t0 = __ldg(p.cu_seqlens + req);
+  d.qlen = __ldg(p.cu_seqlens + req + 1) - d.t0;
+  d.L = __ldg(p.seq_lens + req);
   const int ntq = (d.qlen + QP - 1) / QP;
   d.qpos0 = d.L - d.qlen;
   if (p.prefix_mode) {
     const int segs = prefix_segment_count(d.L, p.kv_splits);
     const int tps = prefix_tiles_per_segment(d.L, p.kv_splits);
-    const int local = u - pref[lo];
     d.seg = local % segs;
     d.j0 = (local / segs) * QP;
     d.j1 = min(d.qlen, d.j0 + QP);
@@ -235,11 +353,11 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const i
     d.n_tiles = min((d.L + kBN - 1) / kBN, d.jb + tps) - d.jb;
     return d;
   }
-  const int qt = ntq - 1 - (u - pref[lo]);  // later (heavier) units first
+  const int qt = ntq - 1 - local;  // later (heavier) units first
   d.j0 = qt * QP;
   d.j1 = min(d.qlen, d.j0 + QP);
   if (p.key_start) {  // key range: the queries' positions come from the caller
-    const int64_t rel = (int64_t)__ldg(p.query_start + lo) - __ldg(p.key_start + lo);
+    const int64_t rel = (int64_t)__ldg(p.query_start + req) - __ldg(p.key_start + req);
     d.qpos0 = (int)max((int64_t)-(1 << 30), min((int64_t)(1 << 30), rel));
   }
   // keys [0, kv_end) are needed; at least one tile runs (fully masked when no
@@ -282,6 +400,56 @@ __device__ __forceinline__ int read_item(Bars* bars, const AttnParams& p, int k,
   return it;
 }
 
+// Two fp32 values as fp16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// acc += both fp16 halves of h (exactly, in fp32).
+__device__ __forceinline__ void add_f16x2_to(float& a, float& b, uint32_t h) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(h));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// One 16-byte piece of a V tile (8 bf16 values) converted in place to fp16
+// (exact for |v| < 65536: fp16 keeps bf16's 8 significant bits); the
+// exponent fields seen are folded into emax (per 16-bit half) for the range
+// check.
+__device__ __forceinline__ void v_piece_to_f16(uint32_t addr, uint32_t& emax) {
+  uint32_t w[4];
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("max.u16x2 %0, %0, %1;" : "+r"(emax) : "r"(w[i] & 0x7f807f80u));
+    w[i] = pack_f16x2(bf16_lo(w[i]), bf16_hi(w[i]));
+  }
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+
+template <int R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 __device__ __forceinline__ void cta_finished(const AttnParams& p) {  // one thread
   __threadfence();
   if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
@@ -291,7 +459,9 @@ __device__ __forceinline__ void cta_finished(const AttnParams& p) {  // one thre
   }
 }
 
-template <int D>
+// F16P: P in fp16 and V converted to fp16 in shared memory (one PV pass);
+// otherwise P as a bf16 high part and remainder (two PV passes, V as stored).
+template <int D, bool F16P>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map, const AttnParams p) {
   using Lay = PrefillLayout<D>;
@@ -300,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + Lay::BAR_OFF);
-  int* pref = reinterpret_cast<int*>(smem + Lay::PREF_OFF);
+  int* list_base = reinterpret_cast<int*>(smem + Lay::PREF_OFF);
 
   griddep_wait();  // the KV write (and all earlier work) has landed
   griddep_launch_dependents();
@@ -318,8 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kNS; ++s) {
       mbar_init(smem_addr(&bars->k_full[s]), kProducers);
       mbar_init(smem_addr(&bars->k_empty[s]), 1);
-      mbar_init(smem_addr(&bars->v_full[s]), kProducers);
+      mbar_init(smem_addr(&bars->v_full[s]), F16P ? kConverters : kProducers);
       mbar_init(smem_addr(&bars->v_empty[s]), 1);
+      mbar_init(smem_addr(&bars->v_landed[s]), kProducers);
     }
     for (int x = 0; x < kQT; ++x) {
       mbar_init(smem_addr(&bars->s_full[x]), 1);
@@ -330,12 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&bars->mma_done), 1);
     for (int k = 0; k < kRing; ++k) {
       mbar_init(smem_addr(&bars->item_full[k]), 1);
-      mbar_init(smem_addr(&bars->item_empty[k]), kItemReaders);
+      mbar_init(smem_addr(&bars->item_empty[k]), item_readers(F16P));
     }
     bars->abort = 0;
     fence_barrier_init();
   }
-  const int total = prefill_prefix(p, pref, bars->scan, QP) * p.num_kv_heads;  // syncs
+  int total_units = 0;
+  const WorkList wl = prefill_work_list(p, list_base, bars->scan, QP, &total_units);  // syncs
+  const int total = total_units * p.num_kv_heads;
   if ((int)blockIdx.x >= total) {  // uniform; nothing allocated yet
     if (threadIdx.x == 0) cta_finished(p);
     return;
@@ -354,26 +527,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t k_s = smem_addr(smem + Lay::K_OFF);
   const uint32_t v_s = smem_addr(smem + Lay::V_OFF);
 
+  // Each role changes its register budget at the top of its own branch (no
+  // control-flow merge between the change and the code that relies on it):
+  // warpgroup 2 (producers) and 3 (MMA + idle warps) give registers back,
+  // warpgroups 0 and 1 (softmax) take them.
   if (warp >= kProdWarp0 && warp < kMmaWarp) {
-    // ===== producers: Q by TMA (one thread), K/V by cp.async (64 threads) =====
-    // Thread pt copies 16-byte piece pc of the rows of keys pk0, pk0 + KSTEP,
-    // ... of every tile into the 128-byte-swizzled layout the MMA descriptors
-    // expect (the piece at column unit u of row r lands at unit u ^ (r & 7)).
-    // Keys past the needed range and rows of bad blocks are filled with
-    // zeros (so V rows there never poison O: P is 0 there, 0 * NaN is not).
+    setmaxnreg_dec<kOtherRegs>();
+    // ===== producers: Q by TMA (one thread); K tiles by cp.async (warps 8-9);
+    // V tiles by cp.async, then converted in place to fp16 (warps 10-11) =====
+    // Thread pt of a role copies 16-byte piece pc of the rows of keys pk0,
+    // pk0 + KSTEP, ... of every tile into the 128-byte-swizzled layout the
+    // MMA descriptors expect (the piece at column unit u of row r lands at
+    // unit u ^ (r & 7)). Keys past the needed range and rows of bad blocks
+    // are filled with zeros (so V rows there never poison O: P is 0 there,
+    // 0 * NaN is not).
     constexpr int RP = D / 8;               // 16-byte pieces per K or V row
     constexpr int KSTEP = kProducers / RP;  // keys per round
     constexpr int NIT = kBN / KSTEP;        // rounds per tile
     static_assert(kSub % KSTEP == 0, "a round stays inside one 16-key sub-block");
-    const int pt = threadIdx.x - kSoftmaxThreads;
+    const bool vrole = warp >= kVWarp0;
+    const int pt = threadIdx.x - (vrole ? kVWarp0 : kProdWarp0) * 32;
     const int pc = pt % RP;
     const int pk0 = pt / RP;
     const uint32_t col_off = (uint32_t)((pc >> 3) * Lay::CH_BYTES);
     const uint32_t pcc = (uint32_t)(pc & 7);
     const int64_t row_bytes = (int64_t)p.num_kv_heads * D * 2;
     const uint8_t* pool = static_cast<const uint8_t*>(p.kv_pool);
-    const int64_t v_half = (int64_t)p.num_blocks * p.block_size * row_bytes;
-    const bool qlead = pt == 0;
+    const int64_t half_off = vrole ? (int64_t)p.num_blocks * p.block_size * row_bytes : 0;
+    const bool qlead = warp == kProdWarp0 && lane == 0;
     if (qlead) prefetch_tmap(&q_map);
     int gi = 0, gt = 0, armed = 0, q_issued = 0;
     bool ok = true, bad_block = false;
@@ -384,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 : read_item(bars, p, gi, abort);
       it = __shfl_sync(kFullMask, it, 0);
       if (it < 0) break;
-      const PrefillItem d = prefill_item(p, pref, QP, it);
+      const PrefillItem d = prefill_item(p, wl, QP, it);
       const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
       if (warp == kProdWarp0) {
         int w = 1;
@@ -411,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int key = (jj * (kBN / kSub) + lane) * kSub;
           ids = (key < d.kv_end) ? __ldg(bt + key / p.block_size) : -1;
         }
-        // byte offset in the K half of the pool of each sub-block's first row
-        // for this thread's piece, or -1 (zero fill)
+        // byte offset in the pool of each sub-block's first row for this
+        // thread's piece, or -1 (zero fill)
         int64_t sub_off[kBN / kSub];
 #pragma unroll
         for (int sb = 0; sb < kBN / kSub; ++sb) {
@@ -423,53 +604,90 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (id < 0 || id >= p.num_blocks)
               bad_block = true;
             else
-              sub_off[sb] = ((int64_t)id * p.block_size + key % p.block_size) * row_bytes + head_off;
+              sub_off[sb] =
+                  half_off + ((int64_t)id * p.block_size + key % p.block_size) * row_bytes + head_off;
           }
         }
         const int st = gt % kNS;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint64_t* empty = half ? &bars->v_empty[st] : &bars->k_empty[st];
-          uint64_t* full = half ? &bars->v_full[st] : &bars->k_full[st];
-          int w = 1;
-          if (lane == 0 && gt >= kNS)
-            w = mbar_wait(smem_addr(empty), ((gt / kNS) - 1) & 1, p.status, abort);
-          ok = __shfl_sync(kFullMask, w, 0) != 0;
-          if (!ok) break;
-          fence_proxy_async_smem();  // the MMAs' reads of this stage precede our writes
-          const uint32_t dst0 = (half ? v_s : k_s) + st * Lay::TILE_BYTES + col_off;
-          const int64_t base = half ? v_half : 0;
-#pragma unroll
-          for (int i = 0; i < NIT; ++i) {
-            const int k = pk0 + KSTEP * i;
-            const int sb = (KSTEP * i) / kSub;
-            const bool valid = sub_off[sb] >= 0 && jj * kBN + k < d.kv_end;
-            const uint8_t* src =
-                valid ? pool + base + sub_off[sb] + (int64_t)(k % kSub) * row_bytes : pool;
-            cp_async_16(dst0 + k * 128 + ((pcc ^ (uint32_t)(k & 7)) << 4), src, valid ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(smem_addr(full));
-        }
+        uint64_t* empty = vrole ? &bars->v_empty[st] : &bars->k_empty[st];
+        uint64_t* full = vrole ? &bars->v_full[st] : &bars->k_full[st];
+        int w = 1;
+        if (lane == 0 && gt >= kNS)
+          w = mbar_wait(smem_addr(empty), ((gt / kNS) - 1) & 1, p.status, abort);
+        ok = __shfl_sync(kFullMask, w, 0) != 0;
         if (!ok) break;
+        fence_proxy_async_smem();  // the MMAs' reads of this stage precede our writes
+        const uint32_t dst0 = (vrole ? v_s : k_s) + st * Lay::TILE_BYTES + col_off;
+#pragma unroll
+        for (int i = 0; i < NIT; ++i) {
+          const int k = pk0 + KSTEP * i;
+          const int sb = (KSTEP * i) / kSub;
+          const bool valid = sub_off[sb] >= 0 && jj * kBN + k < d.kv_end;
+          const uint8_t* src = valid ? pool + sub_off[sb] + (int64_t)(k % kSub) * row_bytes : pool;
+          cp_async_16(dst0 + k * 128 + ((pcc ^ (uint32_t)(k & 7)) << 4), src, valid ? 16u : 0u);
+        }
+        // fp16 P: the V copies go to the converter warps first
+        cp_async_arrive_noinc(smem_addr((F16P && vrole) ? &bars->v_landed[st] : full));
         armed = gt + 1;
       }
+      if (!ok) break;
     }
     if (bad_block) set_status(p.status, PKV_DEV_BAD_BLOCK);
     // our copies, and the barrier arrivals they trigger, land before the CTA can exit
     cp_async_wait_all();
     if (lane == 0) {
-      for (int g = max(0, armed - kNS); g < armed; ++g) {
-        mbar_wait(smem_addr(&bars->k_full[g % kNS]), (g / kNS) & 1, nullptr);
-        mbar_wait(smem_addr(&bars->v_full[g % kNS]), (g / kNS) & 1, nullptr);
-      }
+      uint64_t* landed = vrole ? (F16P ? bars->v_landed : bars->v_full) : bars->k_full;
+      for (int g = max(0, armed - kNS); g < armed; ++g)
+        mbar_wait(smem_addr(&landed[g % kNS]), (g / kNS) & 1, nullptr);
       if (warp == kProdWarp0 && q_issued > 0)
         mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
     }
-  } else if (warp == kMmaWarp) {
-    // ================= MMA issuer (one thread) =================
-    if (lane == 0) {
+  } else if (warp >= kMmaWarp) {
+    setmaxnreg_dec<kOtherRegs>();
+    if (F16P && warp >= kConvWarp0) {
+      // ===== converters (fp16 P): each landed V stage to fp16 in place =====
+      // piece i of a stage (row i / RP, 16-byte column unit i % RP) is
+      // converted by thread i mod 96; the stage is then published to the
+      // tensor core's (async) proxy
+      constexpr int RP = D / 8;
+      const int ct = threadIdx.x - kConvWarp0 * 32;
+      uint32_t emax = 0;  // V exponent fields seen (range check)
+      int gt = 0;
+      bool ok = true;
+      for (int gi = 0; ok; ++gi) {
+        int it = -1;
+        if (lane == 0) it = read_item(bars, p, gi, abort);
+        it = __shfl_sync(kFullMask, it, 0);
+        if (it < 0) break;
+        const PrefillItem d = prefill_item(p, wl, QP, it);
+        for (int j = 0; j < d.n_tiles; ++j, ++gt) {
+          const int st = gt % kNS;
+          int w = 1;
+          if (lane == 0)
+            w = mbar_wait(smem_addr(&bars->v_landed[st]), (gt / kNS) & 1, p.status, abort);
+          ok = __shfl_sync(kFullMask, w, 0) != 0;
+          if (!ok) break;
+          const uint32_t base = v_s + st * Lay::TILE_BYTES;
+#pragma unroll 4
+          for (int i = ct; i < kBN * RP; i += kConverters) {
+            const int k = i / RP, pc = i % RP;
+            v_piece_to_f16(base + (pc >> 3) * Lay::CH_BYTES + k * 128 +
+                               (((uint32_t)(pc & 7) ^ (uint32_t)(k & 7)) << 4),
+                           emax);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(smem_addr(&bars->v_full[st]));
+        }
+      }
+      // a bf16 exponent field >= 143 is a magnitude >= 2^16 (or inf / NaN)
+      if ((emax & 0xffffu) >= 0x4780u || (emax >> 16) >= 0x4780u)
+        set_status(p.status, PKV_DEV_V_RANGE);
+    }
+    // ================= MMA issuer (one thread of warp 12) =================
+    if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, D, false, true);
+      constexpr uint32_t idesc_pv =
+          F16P ? umma_idesc_f16(kBM, D, false, true) : umma_idesc_bf16(kBM, D, false, true);
       bool ok = true;
       int gi = 0, gt = 0;
       // S_x = Q_x K_g^T (the K stage is released after the last Q tile's product)
@@ -488,9 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (x == kQT - 1) umma_commit(smem_addr(&bars->k_empty[g % kNS]));
         umma_commit(smem_addr(&bars->s_full[x]));
       };
-      // O_x += P_x V_g (P as bf16 high parts, then the remainders)
+      // O_x += P_x V_g (fp16 P and V; or bf16 high parts, then the remainders)
       auto issue_pv = [&](int x, int g, bool first) {
-        fence_proxy_async_smem();  // V was written by cp.async (generic proxy)
+        fence_proxy_async_smem();  // V was written by cp.async / st.shared (generic proxy)
         tc_fence_after();
         const uint32_t s_base = tmem + Lay::s_col(x);
         const uint32_t o_base = tmem + Lay::o_col(x);
@@ -498,12 +716,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(o_base, s_base + Lay::p_hi_col(kk), b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          umma_ts(o_base, s_base + (F16P ? Lay::p_col(kk) : Lay::p_hi_col(kk)), b, idesc_pv,
+                  (!first || kk > 0) ? 1u : 0u);
         }
+        if (!F16P) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
+            umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
+          }
         }
         if (x == kQT - 1) umma_commit(smem_addr(&bars->v_empty[g % kNS]));
         umma_commit(smem_addr(&bars->o_done[x]));
@@ -520,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; ok; ++gi) {
         const int it = read_item(bars, p, gi, abort);
         if (it < 0) break;
-        const PrefillItem d = prefill_item(p, pref, QP, it);
+        const PrefillItem d = prefill_item(p, wl, QP, it);
         const int n = d.n_tiles;
         ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
         // S_x is reused after PV of the previous item's last tile: in issue order
@@ -555,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_addr(&bars->mma_done), 0, nullptr);
     }
   } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
     // ====== softmax + epilogue: warpgroup x owns Q tile x, thread r owns row r ======
     const int x = warp >> 2;
     const int r = threadIdx.x & (kBM - 1);
@@ -571,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) it = read_item(bars, p, k, abort);
       it = __shfl_sync(kFullMask, it, 0);
       if (it < 0) break;
-      const PrefillItem d = prefill_item(p, pref, QP, it);
+      const PrefillItem d = prefill_item(p, wl, QP, it);
       const int qj = d.j0 + x * QT + rq;
       const bool row_valid = qj < d.j1;
       // the row's last visible key (a key range may end before the query)
@@ -588,55 +810,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool resc;
         if (__all_sync(kFullMask, lim >= kBN - 1)) {
           // ---- every key of the tile is visible to every row of the warp
-          // pass 1: row maximum (four independent chains)
-          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // pass 1: row maximum (two independent chains of 3-input maxima)
+          float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll 1
           for (int ch = 0; ch < kBN / 32; ++ch) {
             uint32_t u[32];
             PKV_TMEM_LD32(sa + ch * 32, u);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(u[c]));
+            for (int c = 0; c < 16; c += 2) {
+              mxa = max3(mxa, __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
+              mxb = max3(mxb, __uint_as_float(u[2 * c + 2]), __uint_as_float(u[2 * c + 3]));
+            }
           }
-          const float mnew = fmaxf(m, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
+          const float mnew = fmaxf(m, fmaxf(mxa, mxb) * sl2);
           resc = mnew > m + kRescaleThreshold;
           if (resc) {
             alpha = fast_exp2(m - mnew);  // 0 on the first tile
             m = mnew;
           }
-          // pass 2: probabilities in place as packed bf16 hi | lo, where hi
-          // keeps the top 16 bits of p and lo = p - hi (exact) is truncated
-          // the same way: hi + lo is p to 2^-14 relative
           const float2 sl2x2 = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
-          const float2 minus1 = make_float2(-1.f, -1.f);
-          float2 rsa = make_float2(0.f, 0.f), rsb = make_float2(0.f, 0.f);
+          if constexpr (F16P) {
+            // pass 2: probabilities as fp16 pairs, written over the first half
+            // of the chunk's S columns; the row sum adds the rounded values,
+            // so that O and l see the same weights
+            float rsa = 0.f, rsb = 0.f;
 #pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t u[32];
-            PKV_TMEM_LD32(sa + ch * 32, u);
-            tmem_wait_ld();
-            uint32_t pk[32];
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+              uint32_t u[32];
+              PKV_TMEM_LD32(sa + ch * 32, u);
+              tmem_wait_ld();
+              uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float2 x2 = __ffma2_rn(
-                  make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2, negm);
-              const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
-              if (c & 1)
-                rsb = __fadd2_rn(rsb, p2);
-              else
-                rsa = __fadd2_rn(rsa, p2);
-              const uint32_t b0 = __float_as_uint(p2.x), b1 = __float_as_uint(p2.y);
-              const float2 hi2 = make_float2(__uint_as_float(b0 & 0xffff0000u),
-                                             __uint_as_float(b1 & 0xffff0000u));
-              const float2 lo2 = __ffma2_rn(hi2, minus1, p2);
-              pk[c] = __byte_perm(b0, b1, 0x7632);
-              pk[16 + c] = __byte_perm(__float_as_uint(lo2.x), __float_as_uint(lo2.y), 0x7632);
+              for (int c = 0; c < 16; ++c) {
+                const float2 x2 = __ffma2_rn(
+                    make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
+                    negm);
+                pk[c] = pack_f16x2(fast_exp2(x2.x), fast_exp2(x2.y));
+                add_f16x2_to(rsa, rsb, pk[c]);
+              }
+              PKV_TMEM_ST16(sa + ch * 16, pk);
             }
-            PKV_TMEM_ST32(sa + ch * 32, pk);
+            tmem_wait_st();
+            rs = rsa + rsb;
+          } else {
+            // pass 2: probabilities in place as packed bf16 hi | lo, where hi
+            // keeps the top 16 bits of p and lo = p - hi (exact) is truncated
+            // the same way: hi + lo is p to 2^-14 relative
+            const float2 minus1 = make_float2(-1.f, -1.f);
+            float2 rsa = make_float2(0.f, 0.f), rsb = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+              uint32_t u[32];
+              PKV_TMEM_LD32(sa + ch * 32, u);
+              tmem_wait_ld();
+              uint32_t pk[32];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const float2 x2 = __ffma2_rn(
+                    make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
+                    negm);
+                const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+                if (c & 1)
+                  rsb = __fadd2_rn(rsb, p2);
+                else
+                  rsa = __fadd2_rn(rsa, p2);
+                const uint32_t b0 = __float_as_uint(p2.x), b1 = __float_as_uint(p2.y);
+                const float2 hi2 = make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                               __uint_as_float(b1 & 0xffff0000u));
+                const float2 lo2 = __ffma2_rn(hi2, minus1, p2);
+                pk[c] = __byte_perm(b0, b1, 0x7632);
+                pk[16 + c] = __byte_perm(__float_as_uint(lo2.x), __float_as_uint(lo2.y), 0x7632);
+              }
+              PKV_TMEM_ST32(sa + ch * 32, pk);
+            }
+            tmem_wait_st();
+            rs = (rsa.x + rsb.x) + (rsa.y + rsb.y);
           }
-          tmem_wait_st();
-          rs = (rsa.x + rsb.x) + (rsa.y + rsb.y);
         } else {
           // ---- a diagonal tile: hide the keys after each row's position
           // pass 1: row maximum over the visible keys
@@ -657,14 +908,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             alpha = fast_exp2(m - mnew);  // 0 on the first tile
             m = mnew;
           }
-          // pass 2: probabilities, stored in place as packed bf16 hi | lo
-          rs = 0.f;
+          // pass 2: probabilities, stored as fp16 pairs (or bf16 hi | lo)
+          float rsa = 0.f, rsb = 0.f;
 #pragma unroll 1
           for (int ch = 0; ch < kBN / 32; ++ch) {
             uint32_t u[32];
             PKV_TMEM_LD32(sa + ch * 32, u);
             tmem_wait_ld();
-            uint32_t pk[32];
+            uint32_t pk[F16P ? 16 : 32];
             const int vis = lim - ch * 32;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -672,13 +923,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -m));
               if (2 * c > vis) p0 = 0.f;
               if (2 * c + 1 > vis) p1 = 0.f;
-              rs += p0 + p1;
-              pk[c] = pack_bf16x2(p0, p1);
-              pk[16 + c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
+              if constexpr (F16P) {
+                pk[c] = pack_f16x2(p0, p1);
+                add_f16x2_to(rsa, rsb, pk[c]);
+              } else {
+                rsa += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+                pk[16 + c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
+              }
             }
-            PKV_TMEM_ST32(sa + ch * 32, pk);
+            if constexpr (F16P)
+              PKV_TMEM_ST16(sa + ch * 16, pk);
+            else
+              PKV_TMEM_ST32(sa + ch * 32, pk);
           }
           tmem_wait_st();
+          rs = rsa + rsb;
         }
         l = l * alpha + rs;
         if (gg > 0) {
@@ -738,22 +998,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown: all tcgen05 work of the CTA is complete; release TMEM
+  // (its address read again from shared memory: the roles ran with
+  // different register budgets)
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if ((threadIdx.x >> 5) == kMmaWarp) {
+    const Bars* b = reinterpret_cast<const Bars*>(
+        ((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023)) +
+        Lay::BAR_OFF);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(*reinterpret_cast<const volatile uint32_t*>(&b->tmem_base), kTmemCols);
   }
   if (threadIdx.x == 0) cta_finished(p);
 }
+
+#ifndef PKV_PREFILL_F16P
+#define PKV_PREFILL_F16P 1
+#endif
 
 template <int D>
 cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream) {
   using Lay = PrefillLayout<D>;
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kernel = prefill_kernel<D>;
+  auto kernel = prefill_kernel<D, PKV_PREFILL_F16P != 0>;
   static SmemLimit limit;
   if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), 227 * 1024);
       e != cudaSuccess)

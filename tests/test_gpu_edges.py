@@ -244,3 +244,23 @@ def test_public_lse_merge(oracle, P, T, H, D):
     assert np.max(np.abs(o - ref_o)) <= 1e-5
     if fin.any():
         assert np.max(np.abs(l[fin] - ref_l[fin])) <= 1e-5
+
+
+def test_v_beyond_fp16_range_is_flagged(oracle):
+    """The prefill kernel computes P.V in fp16 (exact for |v| < 65536, bf16
+    values converted losslessly); a V value beyond that range in a context it
+    reads sets PKV_DEV_V_RANGE. An ordinary workload never sets it, and a V
+    value at the edge of the range (65280, the largest bf16 below 2^16) does
+    not either."""
+    w = wl.build("vrange", [500, 700], [1, 200], 32, 8, 128, seed=77)
+    for value, flagged in ((0x477F, False), (0x47C3, True)):   # 65280, 100000
+        pool = w.pool.copy()
+        blk = int(w.block_table[1, 3])          # a context block of the prefill request
+        pool[1, blk, 5, 2, 17] = value          # V half, token 5, KV head 2, element 17
+        wv = wl.Workload(**{**w.__dict__, "pool": pool})
+        dev = gu.DeviceStep(wv)
+        dev.write()
+        dev.attend()
+        st = dev.dev_status()
+        assert bool(st & pkv.DEV_V_RANGE) == flagged, st
+        assert st & ~pkv.DEV_V_RANGE == 0
