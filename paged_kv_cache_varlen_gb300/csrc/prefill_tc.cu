@@ -691,20 +691,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int gi = 0, gt = 0;
       // S_x = Q_x K_g^T (the K stage is released after the last Q tile's product)
+      // The thread shares its SM sub-partition with busy softmax warps, so
+      // its instructions per MMA are kept few: descriptors and barrier
+      // addresses are computed once; a k-step only adds its offset (in
+      // 16-byte units) to the start-address field.
+      uint64_t qdesc[kQT], kdesc[kNS], vdesc[kNS];
+      uint32_t k_empty_b[kNS], v_empty_b[kNS], s_full_b[kQT], o_done_b[kQT];
+#pragma unroll
+      for (int x = 0; x < kQT; ++x) {
+        qdesc[x] = smem_desc_sw128(q_s + x * Lay::TILE_BYTES, 16, 1024);
+        s_full_b[x] = smem_addr(&bars->s_full[x]);
+        o_done_b[x] = smem_addr(&bars->o_done[x]);
+      }
+#pragma unroll
+      for (int st = 0; st < kNS; ++st) {
+        kdesc[st] = smem_desc_sw128(k_s + st * Lay::TILE_BYTES, 16, 1024);
+        vdesc[st] = smem_desc_sw128(v_s + st * Lay::TILE_BYTES, Lay::CH_BYTES, 1024);
+        k_empty_b[st] = smem_addr(&bars->k_empty[st]);
+        v_empty_b[st] = smem_addr(&bars->v_empty[st]);
+      }
+      static_assert(kNS == 2 && kQT == 2, "two-way selects below");
       auto issue_qk = [&](int x, int g) {
         fence_proxy_async_smem();  // K was written by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t d_tmem = tmem + Lay::s_col(x);
-        const uint32_t qb = q_s + x * Lay::TILE_BYTES;
-        const uint32_t kb = k_s + (g % kNS) * Lay::TILE_BYTES;
+        const uint64_t qd = x ? qdesc[1] : qdesc[0], kd = (g & 1) ? kdesc[1] : kdesc[0];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Lay::CH_BYTES + (kk & 3) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(qb + off, 16, 1024),
-                  smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+          const uint32_t off16 = ((kk >> 2) * Lay::CH_BYTES + (kk & 3) * 32) >> 4;
+          umma_ss(d_tmem, qd + off16, kd + off16, idesc_qk, kk > 0);
         }
-        if (x == kQT - 1) umma_commit(smem_addr(&bars->k_empty[g % kNS]));
-        umma_commit(smem_addr(&bars->s_full[x]));
+        if (x == kQT - 1) umma_commit((g & 1) ? k_empty_b[1] : k_empty_b[0]);
+        umma_commit(x ? s_full_b[1] : s_full_b[0]);
       };
       // O_x += P_x V_g (fp16 P and V; or bf16 high parts, then the remainders)
       auto issue_pv = [&](int x, int g, bool first) {
@@ -712,22 +730,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t s_base = tmem + Lay::s_col(x);
         const uint32_t o_base = tmem + Lay::o_col(x);
-        const uint32_t v_base = v_s + (g % kNS) * Lay::TILE_BYTES;
+        const uint64_t vd = (g & 1) ? vdesc[1] : vdesc[0];
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-          umma_ts(o_base, s_base + (F16P ? Lay::p_col(kk) : Lay::p_hi_col(kk)), b, idesc_pv,
-                  (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(o_base, s_base + (F16P ? Lay::p_col(kk) : Lay::p_hi_col(kk)),
+                  vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
         if (!F16P) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, Lay::CH_BYTES, 1024);
-            umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, b, idesc_pv, 1u);
-          }
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, vd + (uint32_t)((kk * 16 * 128) >> 4),
+                    idesc_pv, 1u);
         }
-        if (x == kQT - 1) umma_commit(smem_addr(&bars->v_empty[g % kNS]));
-        umma_commit(smem_addr(&bars->o_done[x]));
+        if (x == kQT - 1) umma_commit((g & 1) ? v_empty_b[1] : v_empty_b[0]);
+        umma_commit(x ? o_done_b[1] : o_done_b[0]);
       };
       // Fixed issue order per item: QK_A(0), QK_B(0), then for every tile j
       // PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1). After the first tile this
