@@ -14,10 +14,12 @@
  * ---------------------------------------
  * - All tensor pointers are DEVICE pointers owned by the caller. The library
  *   never allocates device memory, never frees it, never synchronises the
- *   stream and keeps no state between calls, with two stated exceptions: the
- *   built-in scratch array of pkv_paged_attention_varlen_noalloc and the
+ *   stream and keeps no state between calls, with stated exceptions: the
+ *   built-in scratch array of pkv_paged_attention_varlen_noalloc, the
  *   host-side block manager objects (pkv_bm_*), which the caller creates and
- *   destroys.
+ *   destroys, and one side stream with two events per device and host
+ *   thread that the attention calls create on first use (see
+ *   pkv_paged_attention_varlen).
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream). A call returns as soon as the
  *   kernels are queued.
@@ -155,7 +157,13 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  * tensor cores).
  * The kernels use programmatic dependent launch: each waits for the grid
  * before it in the stream to finish before touching memory, so ordinary
- * stream order holds.
+ * stream order holds. A batch with requests for both kernels runs them side
+ * by side: the prefill grid on `stream` (at the device's highest launch
+ * priority), the decode grids on a low-priority side stream that the library
+ * creates once per device and host thread (with two events), forked from
+ * `stream` at the start of the call and joined back into it at the end, so
+ * the call is still ordered in `stream` as a whole (and records into a CUDA
+ * graph as a fork and a join).
  */
 pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
                                       const void *kv_pool, const int32_t *block_table,

@@ -2,8 +2,9 @@
 // argument validation, TMA tensor-map encoding and kernel dispatch.
 //
 // Nothing here allocates device memory, synchronises a stream or keeps
-// state across calls (the only cached items are the driver entry point of
-// cuTensorMapEncodeTiled and, per device, the kernels' shared-memory limits).
+// state across calls (the cached items are the driver entry point of
+// cuTensorMapEncodeTiled, per device the kernels' shared-memory limits, and
+// per device and host thread one side stream with two events).
 // Every host-side check and tensor-map encoding of a call happens before its
 // first launch, so a rejected call enqueues nothing.
 #include <cuda.h>
@@ -287,9 +288,64 @@ pkv_status bind_workspace(AttnPlan* a, void* workspace, size_t workspace_bytes) 
   return PKV_OK;
 }
 
-// Enqueue a planned call: the decode grid (and its split-KV merge grid), then
+// A side stream at the device's lowest priority and two events per device
+// and host thread, created on first use and kept until the process exits:
+// they let one call run its prefill and decode grids side by side (fork /
+// join inside the call).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  int greatest_priority = 0;
+};
+
+cudaError_t side_stream(SideStream** out) {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_device[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& ss = per_device[dev];
+  if (!ss.join) {
+    int least = 0, greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+    ss.greatest_priority = greatest;
+    if (!ss.stream &&
+        (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, least)) !=
+            cudaSuccess)
+      return e;
+    if (!ss.fork && (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) !=
+                        cudaSuccess)
+      return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
+// Enqueue a planned call: the decode grid (and its split-KV merge grid), and
 // the prefill grid when some request is longer than the decode kernel takes.
-pkv_status launch_plan(const AttnPlan& a, cudaStream_t st) {
+// With both, and `fork` set, the two run side by side: the prefill grid on
+// the caller's stream at the device's highest launch priority (so that its
+// one-CTA-per-SM persistent grid takes the SMs first), the decode grids on
+// the low-priority side stream behind an event recorded before it, their
+// CTAs filling the SMs that the prefill's last work items leave idle; the
+// caller's stream then waits for the side stream, so the call still
+// completes only when every grid has. Otherwise the grids run one after the
+// other on the caller's stream.
+pkv_status launch_plan(const AttnPlan& a, cudaStream_t st, bool fork = true) {
+  if (a.prefill && fork) {
+    SideStream* ss = nullptr;
+    if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_prefill(a.p, a.q_map, st, ss->greatest_priority) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_decode_mma(a.p, a.kv_rows, ss->stream) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess) return PKV_ERR_CUDA;
+    return cudaStreamWaitEvent(st, ss->join, 0) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   if (pkv::launch_decode_mma(a.p, a.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
   if (a.prefill && pkv::launch_prefill(a.p, a.q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
@@ -322,7 +378,8 @@ pkv_status attention_with_scratch(float* out, float* out_lse, const void* q, con
   // the work tickets must start at zero (an interrupted earlier call may
   // have left them otherwise)
   if (cudaMemsetAsync(a.p.sched, 0, kSchedBytes, st) != cudaSuccess) return PKV_ERR_CUDA;
-  return launch_plan(a, st);
+  // one stream only: a side stream would be a resource created on first use
+  return launch_plan(a, st, false);
 }
 
 }  // namespace pkv

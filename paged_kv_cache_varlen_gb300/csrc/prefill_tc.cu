@@ -1033,7 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
 template <int D>
-cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream) {
+cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream,
+                             int priority) {
   using Lay = PrefillLayout<D>;
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -1055,19 +1056,22 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cuda
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = priority;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = priority != 0 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, q_map, p);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream) {
-  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, stream);
-  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, stream);
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream,
+                           int priority) {
+  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, stream, priority);
+  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, stream, priority);
   return cudaErrorInvalidValue;
 }
 
