@@ -118,9 +118,10 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t he
 }
 
 // Shared-prefix (cascade) decode: key segments per prefix so that the
-// prefix pass spreads over about a GPU's worth of CTAs (148 is a reference
-// count; the results do not depend on it).
-constexpr int64_t kCascadeRefSMs = 148;
+// prefix pass spreads over about a quarter of a GPU's SMs (38 CTAs of its
+// one-per-SM grid; the results do not depend on it): it runs beside the
+// tail decode, which keeps the other SMs busy from the start.
+constexpr int64_t kCascadeRefSMs = 38;
 
 int32_t cascade_splits(int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len,
                        int32_t num_heads, int32_t num_kv_heads) {
@@ -591,10 +592,23 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
   if (pkv::launch_cascade_prepare(part_lse, (int64_t)c.splits * bh, tail_cu, num_seqs, st) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
-  // 2. tails
-  if ((s = launch_plan(tails, st)) != PKV_OK) return s;
-  // 3. prefixes
-  if (prefixes && pkv::launch_prefill(p, q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (prefixes) {
+    // 2 + 3. the prefix pass (tensor cores, on `st` at the highest launch
+    // priority) and the tails (decode kernel, on the side stream) run side
+    // by side; they write disjoint partial slots
+    SideStream* ss = nullptr;
+    if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_prefill(p, q_map, st, ss->greatest_priority) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
+    if ((s = launch_plan(tails, ss->stream)) != PKV_OK) return s;
+    if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  } else if ((s = launch_plan(tails, st)) != PKV_OK) {  // 2. tails only
+    return s;
+  }
   // 4. merge every request's prefix segments and tail by log-sum-exp
   return pkv::launch_lse_merge(out, out_lse, part_out, part_lse, c.splits + 1, bh, head_dim, st) ==
                  cudaSuccess
