@@ -48,6 +48,15 @@
 #include "common.cuh"
 #include "launch.h"
 
+#ifdef PKV_TEST_HOLD_ARRIVAL
+// Test builds only: while set, warp 0 of the first CTA withholds the copy of
+// its second chunk, so that its bounded wait on that chunk runs out.
+__device__ int g_pkv_test_hold_decode;
+extern "C" int pkv_test_hold_decode(int on) {
+  return (int)cudaMemcpyToSymbol(g_pkv_test_hold_decode, &on, sizeof(int));
+}
+#endif
+
 namespace pkv {
 namespace {
 
@@ -199,6 +208,13 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   int issued = 0;
   for (int k = 0; k < SPW && k < my_chunks; ++k) {
     const int32_t id = __shfl_sync(kFull, ids_cur, k);
+#ifdef PKV_TEST_HOLD_ARRIVAL
+    if (g_pkv_test_hold_decode && k == 1 && warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+        blockIdx.z == 0) {
+      ++issued;  // counted as issued: the drain below waits for it (and gives up)
+      continue;
+    }
+#endif
     if (lane == 0) issue(k, id);
     ++issued;
   }

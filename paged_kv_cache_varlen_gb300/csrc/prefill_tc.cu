@@ -60,6 +60,15 @@
 #include "common.cuh"
 #include "launch.h"
 
+#ifdef PKV_TEST_HOLD_ARRIVAL
+// Test builds only: while set, softmax warp 0 of CTA 0 withholds its P-ready
+// arrival for its first tile, so that the MMA thread's bounded wait runs out.
+__device__ int g_pkv_test_hold_prefill;
+extern "C" int pkv_test_hold_prefill(int on) {
+  return (int)cudaMemcpyToSymbol(g_pkv_test_hold_prefill, &on, sizeof(int));
+}
+#endif
+
 namespace pkv {
 namespace {
 
@@ -977,6 +986,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();  // the warp's P (and O) stores precede its one arrival
+#ifdef PKV_TEST_HOLD_ARRIVAL
+        if (g_pkv_test_hold_prefill && blockIdx.x == 0 && warp == 0 && gg == 0) continue;
+#endif
         if (lane == 0) mbar_arrive(smem_addr(&bars->p_ready[x]));
       }
       if (!ok) break;
