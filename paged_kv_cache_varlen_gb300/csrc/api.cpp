@@ -169,6 +169,7 @@ struct AttnPlan {
   AttnParams p{};
   CUtensorMap kv_rows{};  // decode: 16-key boxes of whole rows of one KV head
   CUtensorMap q_map{};    // prefill: {64, G, 128/G} boxes of q
+  CUtensorMap kv_box{};   // prefill: 16-key boxes of one 64-column chunk
   bool prefill = false;   // some request may have more queries than the decode kernel takes
   bool empty = false;
   WorkspaceLayout wl{};
@@ -251,26 +252,42 @@ pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q
   return PKV_OK;
 }
 
+// The pool [2][NB][BS][Hkv][D] viewed as [D/64][Hkv][2*NB*BS rows][64]
+// (strides 128 B, D*2, Hkv*D*2; the V half starts at row NB*BS), 128-byte
+// swizzle, with a box of 16 rows of one KV head and `chunks` 64-column
+// chunks. With all D/64 chunks (decode) the box lands as the 16 keys' first
+// 128-byte halves, then their second halves: 8 consecutive keys of one half
+// then sit in 8 different bank groups (conflict-free ldmatrix). With one
+// chunk (prefill) each copy lands 16 rows of one chunk of a 128-key tile.
+bool encode_kv_view(CUtensorMap* map, const void* kv_pool, int32_t num_blocks, int32_t block_size,
+                    int32_t num_kv_heads, int32_t head_dim, uint32_t chunks) {
+  const uint64_t D = (uint64_t)head_dim;
+  const uint64_t pool_rows = (uint64_t)2 * num_blocks * block_size;
+  const uint64_t dims[4] = {64, pool_rows, (uint64_t)num_kv_heads, D / 64};
+  const uint64_t strides[3] = {(uint64_t)num_kv_heads * D * 2, D * 2, 128};
+  const uint32_t box[4] = {64, 16, 1, chunks};
+  return encode_4d(map, kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// q [T][H][D] with a box of {64, G, 128/G} (one 128-row Q tile per chunk).
+bool encode_q_tiles(CUtensorMap* map, const void* q, int32_t num_tokens, int32_t num_heads,
+                    int32_t num_kv_heads, int32_t head_dim) {
+  const uint64_t D = (uint64_t)head_dim;
+  const int32_t group = num_heads / num_kv_heads;
+  return encode_3d(map, q, D, num_heads, num_tokens, D * 2, (uint64_t)num_heads * D * 2, 64,
+                   (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // Encode the plan's TMA tensor maps (needs the driver; still enqueues nothing).
 pkv_status encode_plan(AttnPlan* a) {
   const AttnParams& p = a->p;
-  const uint64_t D = (uint64_t)p.head_dim;
-  const uint64_t pool_rows = (uint64_t)2 * p.num_blocks * p.block_size;
-  // decode: a 16-key box of whole rows of one KV head, the pool viewed as
-  // [D/64][Hkv][rows][64] (strides 128 B, D*2, Hkv*D*2) so that the box
-  // lands as the 16 keys' first 128-byte halves, then their second halves:
-  // with the 128-byte swizzle, 8 consecutive keys of one half then sit in 8
-  // different bank groups (conflict-free ldmatrix)
-  const uint64_t dims[4] = {64, pool_rows, (uint64_t)p.num_kv_heads, D / 64};
-  const uint64_t strides[3] = {(uint64_t)p.num_kv_heads * D * 2, D * 2, 128};
-  const uint32_t box[4] = {64, 16, 1, (uint32_t)(D / 64)};
-  if (!encode_4d(&a->kv_rows, p.kv_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_kv_view(&a->kv_rows, p.kv_pool, p.num_blocks, p.block_size, p.num_kv_heads,
+                      p.head_dim, (uint32_t)(p.head_dim / 64)))
     return PKV_ERR_CUDA;
-  const int32_t group = p.num_heads / p.num_kv_heads;
   if (a->prefill &&
-      !encode_3d(&a->q_map, p.q, D, p.num_heads, p.num_tokens, D * 2,
-                 (uint64_t)p.num_heads * D * 2, 64, (uint32_t)group, (uint32_t)(128 / group),
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+      (!encode_q_tiles(&a->q_map, p.q, p.num_tokens, p.num_heads, p.num_kv_heads, p.head_dim) ||
+       !encode_kv_view(&a->kv_box, p.kv_pool, p.num_blocks, p.block_size, p.num_kv_heads,
+                       p.head_dim, 1)))
     return PKV_ERR_CUDA;
   return PKV_OK;
 }
@@ -340,7 +357,7 @@ pkv_status launch_plan(const AttnPlan& a, cudaStream_t st, bool fork = true) {
     SideStream* ss = nullptr;
     if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(a.p, a.q_map, st, ss->greatest_priority) != cudaSuccess)
+    if (pkv::launch_prefill(a.p, a.q_map, a.kv_box, st, ss->greatest_priority) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
     if (pkv::launch_decode_mma(a.p, a.kv_rows, ss->stream) != cudaSuccess) return PKV_ERR_CUDA;
@@ -348,7 +365,8 @@ pkv_status launch_plan(const AttnPlan& a, cudaStream_t st, bool fork = true) {
     return cudaStreamWaitEvent(st, ss->join, 0) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   }
   if (pkv::launch_decode_mma(a.p, a.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
-  if (a.prefill && pkv::launch_prefill(a.p, a.q_map, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (a.prefill && pkv::launch_prefill(a.p, a.q_map, a.kv_box, st) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return PKV_OK;
 }
 
@@ -559,7 +577,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
   // tensor cores (the prefill kernel in prefix mode), cut into key segments.
   const bool prefixes = num_prefix_groups > 0 && max_prefix_len > 0;
   AttnParams p = tails.p;
-  CUtensorMap q_map{};
+  CUtensorMap q_map{}, kv_box{};
   if (prefixes) {
     p.out = part_out;
     p.out_lse = part_lse;
@@ -582,9 +600,8 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     p.kv_splits = c.splits;
     p.split_out_stride = bh * head_dim;
     p.split_lse_stride = bh;
-    const uint64_t D = (uint64_t)head_dim;
-    if (!encode_3d(&q_map, q, D, num_heads, num_seqs, D * 2, (uint64_t)num_heads * D * 2, 64,
-                   (uint32_t)group, (uint32_t)(128 / group), CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_q_tiles(&q_map, q, num_seqs, num_heads, num_kv_heads, head_dim) ||
+        !encode_kv_view(&kv_box, kv_pool, num_blocks, block_size, num_kv_heads, head_dim, 1))
       return PKV_ERR_CUDA;
   }
 
@@ -599,7 +616,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     SideStream* ss = nullptr;
     if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(p, q_map, st, ss->greatest_priority) != cudaSuccess)
+    if (pkv::launch_prefill(p, q_map, kv_box, st, ss->greatest_priority) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
     if ((s = launch_plan(tails, ss->stream)) != PKV_OK) return s;

@@ -171,6 +171,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tcgen05) accesses of the same memory.
+// 16 zero bytes to shared memory.
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -113,11 +113,12 @@ cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
 
 // Chunked-prefill kernel (query_len > 1 requests), tcgen05 tensor cores.
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle.
-// K/V pages are gathered through p.kv_pool.
+// `kv_map`: the pool viewed as for the decode kernel but with a box of
+// {64, 16, 1, 1} (one 64-column chunk of 16 keys), 128-byte swizzle.
 // `priority` (0: the stream's own) is the launch's scheduling priority, a
 // value in the device's stream-priority range (lower runs first).
-cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream,
-                           int priority = 0);
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
+                           const CUtensorMap& kv_map, cudaStream_t stream, int priority = 0);
 
 // Cascade preparation: part_lse[0 .. n_lse) = -inf and tail_cu[i] = i for
 // i <= num_seqs.

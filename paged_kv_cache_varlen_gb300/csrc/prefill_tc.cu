@@ -76,12 +76,11 @@ constexpr int kBM = 128;                             // Q rows per tile
 constexpr int kQT = 2;                               // Q tiles per work item
 constexpr int kBN = 128;                             // keys per KV tile
 constexpr int kNS = 2;                               // stages of each of the K and V rings
-constexpr int kSub = 16;                             // keys per gathered sub-block
+constexpr int kSub = 16;                             // keys per TMA box
 constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 7 (warpgroups 0, 1)
-constexpr int kProducers = 64;                       // threads of each producer role
-constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warps 8-9: K tiles (warp 8 also Q)
-constexpr int kVWarp0 = kProdWarp0 + kProducers / 32;  // warps 10-11: V tiles, to fp16
-constexpr int kMmaWarp = kVWarp0 + kProducers / 32;  // warp 12
+constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warp 8: Q and K tiles (warp 9 idle)
+constexpr int kVWarp0 = kProdWarp0 + 2;              // warp 10: V tiles (warp 11 idle)
+constexpr int kMmaWarp = kVWarp0 + 2;                // warp 12
 constexpr int kConvWarp0 = kMmaWarp + 1;             // warps 13-15: V to fp16 (fp16 P only)
 constexpr int kConverters = 3 * 32;
 constexpr int kThreads = 512;                        // four warpgroups
@@ -93,11 +92,9 @@ static_assert(2 * kSoftmaxRegs + 2 * kOtherRegs == 4 * (65536 / kThreads),
               "the register split adds up to the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRing = 4;  // work items announced ahead of the roles that consume them
-// readers of an announced item: producer warps 9-11, the MMA thread, the
-// eight softmax warps (one lane each) and, with fp16 P, the three converter warps
-__host__ __device__ constexpr int item_readers(bool f16p) {
-  return 3 + 1 + kSoftmaxThreads / 32 + (f16p ? 3 : 0);
-}
+// readers of an announced item: the V producer warp, the MMA thread, the
+// eight softmax warps and the three converter warps (one lane each)
+constexpr int kItemReaders = 1 + 1 + kSoftmaxThreads / 32 + 3;
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
 
@@ -132,13 +129,8 @@ struct PrefillLayout {
   // TMEM columns: S of tile x (P written in place), then O of tile x
   __device__ static constexpr uint32_t s_col(int x) { return 128u * (uint32_t)x; }
   __device__ static constexpr uint32_t o_col(int x) { return 128u * (uint32_t)(kQT + x); }
-  // P of keys 16*kk .. 16*kk+15 inside an S buffer. fp16 P: pairs in 8
-  // columns. bf16 P: each 32-key piece holds 16 columns of packed high parts
-  // then 16 columns of packed remainders.
+  // P of keys 16*kk .. 16*kk+15 inside an S buffer: fp16 pairs in 8 columns
   __device__ static constexpr uint32_t p_col(int kk) { return 8u * (uint32_t)kk; }
-  __device__ static constexpr uint32_t p_hi_col(int kk) {
-    return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
-  }
 };
 static_assert(kQT * 2 * 128 <= (int)kTmemCols, "S and O of every Q tile fit in TMEM");
 
@@ -146,7 +138,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kNS], k_empty[kNS];
   uint64_t v_full[kNS], v_empty[kNS];
-  uint64_t v_landed[kNS];  // fp16 P: V copies arrived (bf16), not yet converted
+  uint64_t v_landed[kNS];  // V copies arrived (bf16), not yet converted
   uint64_t s_full[kQT];   // QK^T of the tile landed in S_x
   uint64_t p_ready[kQT];  // the warpgroup stored P_x (and rescaled O_x)
   uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
@@ -157,6 +149,7 @@ struct Bars {
   uint32_t tmem_base;
   int32_t abort;
   int32_t scan[kThreads / 32];
+  uint32_t v_mask[kNS];  // boxes of the V stage that were loaded (bit b: keys 16b .. 16b+15)
 };
 
 struct PrefillItem {
@@ -468,11 +461,10 @@ __device__ __forceinline__ void cta_finished(const AttnParams& p) {  // one thre
   }
 }
 
-// F16P: P in fp16 and V converted to fp16 in shared memory (one PV pass);
-// otherwise P as a bf16 high part and remainder (two PV passes, V as stored).
-template <int D, bool F16P>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap q_map, const AttnParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
   using Lay = PrefillLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
@@ -495,11 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&bars->q_full), 1);
     mbar_init(smem_addr(&bars->q_empty), 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(smem_addr(&bars->k_full[s]), kProducers);
+      mbar_init(smem_addr(&bars->k_full[s]), 1);  // the producer's arrival + TMA bytes
       mbar_init(smem_addr(&bars->k_empty[s]), 1);
-      mbar_init(smem_addr(&bars->v_full[s]), F16P ? kConverters : kProducers);
+      mbar_init(smem_addr(&bars->v_full[s]), kConverters);
       mbar_init(smem_addr(&bars->v_empty[s]), 1);
-      mbar_init(smem_addr(&bars->v_landed[s]), kProducers);
+      mbar_init(smem_addr(&bars->v_landed[s]), 1);
     }
     for (int x = 0; x < kQT; ++x) {
       mbar_init(smem_addr(&bars->s_full[x]), 1);
@@ -510,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&bars->mma_done), 1);
     for (int k = 0; k < kRing; ++k) {
       mbar_init(smem_addr(&bars->item_full[k]), 1);
-      mbar_init(smem_addr(&bars->item_empty[k]), item_readers(F16P));
+      mbar_init(smem_addr(&bars->item_empty[k]), kItemReaders);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -542,122 +534,121 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warpgroups 0 and 1 (softmax) take them.
   if (warp >= kProdWarp0 && warp < kMmaWarp) {
     setmaxnreg_dec<kOtherRegs>();
-    // ===== producers: Q by TMA (one thread); K tiles by cp.async (warps 8-9);
-    // V tiles by cp.async, then converted in place to fp16 (warps 10-11) =====
-    // Thread pt of a role copies 16-byte piece pc of the rows of keys pk0,
-    // pk0 + KSTEP, ... of every tile into the 128-byte-swizzled layout the
-    // MMA descriptors expect (the piece at column unit u of row r lands at
-    // unit u ^ (r & 7)). Keys past the needed range and rows of bad blocks
-    // are filled with zeros (so V rows there never poison O: P is 0 there,
-    // 0 * NaN is not).
-    constexpr int RP = D / 8;               // 16-byte pieces per K or V row
-    constexpr int KSTEP = kProducers / RP;  // keys per round
-    constexpr int NIT = kBN / KSTEP;        // rounds per tile
-    static_assert(kSub % KSTEP == 0, "a round stays inside one 16-key sub-block");
-    const bool vrole = warp >= kVWarp0;
-    const int pt = threadIdx.x - (vrole ? kVWarp0 : kProdWarp0) * 32;
-    const int pc = pt % RP;
-    const int pk0 = pt / RP;
-    const uint32_t col_off = (uint32_t)((pc >> 3) * Lay::CH_BYTES);
-    const uint32_t pcc = (uint32_t)(pc & 7);
-    const int64_t row_bytes = (int64_t)p.num_kv_heads * D * 2;
-    const uint8_t* pool = static_cast<const uint8_t*>(p.kv_pool);
-    const int64_t half_off = vrole ? (int64_t)p.num_blocks * p.block_size * row_bytes : 0;
-    const bool qlead = warp == kProdWarp0 && lane == 0;
-    if (qlead) prefetch_tmap(&q_map);
-    int gi = 0, gt = 0, armed = 0, q_issued = 0;
-    bool ok = true, bad_block = false;
-    for (;; ++gi) {
-      int it = -1;
-      if (lane == 0)
-        it = warp == kProdWarp0 ? take_item(bars, p, total, gi, abort)
-                                : read_item(bars, p, gi, abort);
-      it = __shfl_sync(kFullMask, it, 0);
-      if (it < 0) break;
-      const PrefillItem d = prefill_item(p, wl, QP, it);
-      const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
-      if (warp == kProdWarp0) {
-        int w = 1;
-        if (lane == 0 && gi >= 1)  // the previous item's QK^T products are done with Q
-          w = mbar_wait(smem_addr(&bars->q_empty), (gi - 1) & 1, p.status, abort);
-        ok = __shfl_sync(kFullMask, w, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          // rows past the last token read as zeros; rows of the next request
-          // are loaded but belong to no valid output row
-          mbar_arrive_expect_tx(smem_addr(&bars->q_full), kQT * Lay::TILE_BYTES);
-          for (int x = 0; x < kQT; ++x)
-            for (int c = 0; c < Lay::NCH; ++c)
-              tma_load_3d(q_s + x * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
-                          smem_addr(&bars->q_full), c * 64, d.kvh * G, d.t0 + d.j0 + x * QT);
-        }
-        ++q_issued;
+    // ===== producers: Q (warp 8) and the K tiles (warp 8), the V tiles (warp
+    // 10), all by TMA; warps 9 and 11 have no work =====
+    // A 128-key tile is 8 boxes of 16 keys (a 16-key run never crosses a
+    // page: block_size is a multiple of 16), each box one TMA copy per
+    // 64-column chunk, landing 128-byte-swizzled in the layout the MMA
+    // descriptors read. Boxes wholly past the needed keys, or in a page
+    // whose id is bad, are not loaded: K rows there are masked by the
+    // softmax (bad-block K rows are zeroed here), V rows are zeroed by the
+    // converter warps (P is 0 there, but 0 * NaN is not 0).
+    if (warp == kProdWarp0 || warp == kVWarp0) {
+      const bool vrole = warp == kVWarp0;
+      const int32_t half_rows = vrole ? p.num_blocks * p.block_size : 0;  // first V row of the view
+      const uint32_t ring = vrole ? v_s : k_s;
+      if (lane == 0) {
+        prefetch_tmap(&kv_map);
+        if (!vrole) prefetch_tmap(&q_map);
       }
-      const int64_t head_off = (int64_t)d.kvh * D * 2 + pc * 16;
-      int32_t ids = -1;
-      for (int j = 0; j < d.n_tiles; ++j, ++gt) {
-        const int jj = d.jb + j;  // key tile
-        if ((j & 3) == 0) {  // block ids of the next 4 tiles, one 16-key sub-block per lane
-          const int key = (jj * (kBN / kSub) + lane) * kSub;
-          ids = (key < d.kv_end) ? __ldg(bt + key / p.block_size) : -1;
-        }
-        // byte offset in the pool of each sub-block's first row for this
-        // thread's piece, or -1 (zero fill)
-        int64_t sub_off[kBN / kSub];
-#pragma unroll
-        for (int sb = 0; sb < kBN / kSub; ++sb) {
-          const int32_t id = __shfl_sync(kFullMask, ids, (j & 3) * (kBN / kSub) + sb);
-          const int key = jj * kBN + sb * kSub;
-          sub_off[sb] = -1;
-          if (key < d.kv_end) {
-            if (id < 0 || id >= p.num_blocks)
-              bad_block = true;
-            else
-              sub_off[sb] =
-                  half_off + ((int64_t)id * p.block_size + key % p.block_size) * row_bytes + head_off;
+      int gi = 0, gt = 0, armed = 0, q_issued = 0;
+      bool ok = true, bad_block = false;
+      for (;; ++gi) {
+        int it = -1;
+        if (lane == 0)
+          it = vrole ? read_item(bars, p, gi, abort) : take_item(bars, p, total, gi, abort);
+        it = __shfl_sync(kFullMask, it, 0);
+        if (it < 0) break;
+        const PrefillItem d = prefill_item(p, wl, QP, it);
+        const int32_t* bt = p.block_table + (int64_t)d.req * p.max_blocks;
+        if (!vrole) {
+          int w = 1;
+          if (lane == 0 && gi >= 1)  // the previous item's QK^T products are done with Q
+            w = mbar_wait(smem_addr(&bars->q_empty), (gi - 1) & 1, p.status, abort);
+          ok = __shfl_sync(kFullMask, w, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) {
+            // rows past the last token read as zeros; rows of the next request
+            // are loaded but belong to no valid output row
+            mbar_arrive_expect_tx(smem_addr(&bars->q_full), kQT * Lay::TILE_BYTES);
+            for (int x = 0; x < kQT; ++x)
+              for (int c = 0; c < Lay::NCH; ++c)
+                tma_load_3d(q_s + x * Lay::TILE_BYTES + c * Lay::CH_BYTES, &q_map,
+                            smem_addr(&bars->q_full), c * 64, d.kvh * G, d.t0 + d.j0 + x * QT);
           }
+          ++q_issued;
         }
-        const int st = gt % kNS;
-        uint64_t* empty = vrole ? &bars->v_empty[st] : &bars->k_empty[st];
-        uint64_t* full = vrole ? &bars->v_full[st] : &bars->k_full[st];
-        int w = 1;
-        if (lane == 0 && gt >= kNS)
-          w = mbar_wait(smem_addr(empty), ((gt / kNS) - 1) & 1, p.status, abort);
-        ok = __shfl_sync(kFullMask, w, 0) != 0;
-        if (!ok) break;
-        fence_proxy_async_smem();  // the MMAs' reads of this stage precede our writes
-        const uint32_t dst0 = (vrole ? v_s : k_s) + st * Lay::TILE_BYTES + col_off;
+        int32_t ids = -1;
+        for (int j = 0; j < d.n_tiles; ++j, ++gt) {
+          const int jj = d.jb + j;  // key tile
+          if ((j & 3) == 0) {  // block ids of the next 4 tiles, one 16-key box per lane
+            const int key = (jj * (kBN / kSub) + lane) * kSub;
+            ids = (key < d.kv_end) ? __ldg(bt + key / p.block_size) : -1;
+          }
+          // lane b < 8: box b of the tile -- loaded or not, and its first row
+          const int b = lane & 7;
+          const int32_t id = __shfl_sync(kFullMask, ids, (j & 3) * (kBN / kSub) + b);
+          const int key = jj * kBN + b * kSub;
+          const bool in_range = lane < 8 && key < d.kv_end;
+          const bool good = in_range && id >= 0 && id < p.num_blocks;
+          bad_block |= in_range && !good;
+          const uint32_t load = __ballot_sync(kFullMask, good);
+          const uint32_t zero = vrole ? 0u : __ballot_sync(kFullMask, in_range && !good);
+          const int32_t row = good ? half_rows + id * p.block_size + key % p.block_size : 0;
+          const int st = gt % kNS;
+          uint64_t* empty = vrole ? &bars->v_empty[st] : &bars->k_empty[st];
+          uint64_t* full = vrole ? &bars->v_landed[st] : &bars->k_full[st];
+          int w = 1;
+          if (lane == 0 && gt >= kNS)
+            w = mbar_wait(smem_addr(empty), ((gt / kNS) - 1) & 1, p.status, abort);
+          ok = __shfl_sync(kFullMask, w, 0) != 0;
+          if (!ok) break;
+          const uint32_t dst0 = ring + st * Lay::TILE_BYTES;
+          if (zero) {  // K rows of a bad page read as zeros
+            fence_proxy_async_smem();
+            constexpr int UNITS = Lay::NCH * kSub * 8;  // 16-byte units of one box
+            for (int i = lane; i < (kBN / kSub) * UNITS; i += 32) {
+              const int bx = i / UNITS, u = i % UNITS;
+              if ((zero >> bx) & 1)
+                st_shared_zero16(dst0 + (u / (kSub * 8)) * Lay::CH_BYTES + bx * kSub * 128 +
+                                 (u % (kSub * 8)) * 16);
+            }
+            fence_proxy_async_smem();
+          }
+          if (vrole && lane == 0) *reinterpret_cast<volatile uint32_t*>(&bars->v_mask[st]) = load;
+          __syncwarp();
+          if (lane == 0)
+            mbar_arrive_expect_tx(smem_addr(full), __popc(load) * Lay::NCH * kSub * 128);
 #pragma unroll
-        for (int i = 0; i < NIT; ++i) {
-          const int k = pk0 + KSTEP * i;
-          const int sb = (KSTEP * i) / kSub;
-          const bool valid = sub_off[sb] >= 0 && jj * kBN + k < d.kv_end;
-          const uint8_t* src = valid ? pool + sub_off[sb] + (int64_t)(k % kSub) * row_bytes : pool;
-          cp_async_16(dst0 + k * 128 + ((pcc ^ (uint32_t)(k & 7)) << 4), src, valid ? 16u : 0u);
+          for (int bb = 0; bb < kBN / kSub; ++bb) {
+            const int32_t r = __shfl_sync(kFullMask, row, bb);
+            if (lane == 0 && ((load >> bb) & 1))
+              for (int c = 0; c < Lay::NCH; ++c)
+                tma_load_4d(dst0 + c * Lay::CH_BYTES + bb * kSub * 128, &kv_map, smem_addr(full), 0,
+                            r, d.kvh, c);
+          }
+          armed = gt + 1;
         }
-        // fp16 P: the V copies go to the converter warps first
-        cp_async_arrive_noinc(smem_addr((F16P && vrole) ? &bars->v_landed[st] : full));
-        armed = gt + 1;
+        if (!ok) break;
       }
-      if (!ok) break;
-    }
-    if (bad_block) set_status(p.status, PKV_DEV_BAD_BLOCK);
-    // our copies, and the barrier arrivals they trigger, land before the CTA can exit
-    cp_async_wait_all();
-    if (lane == 0) {
-      uint64_t* landed = vrole ? (F16P ? bars->v_landed : bars->v_full) : bars->k_full;
-      for (int g = max(0, armed - kNS); g < armed; ++g)
-        mbar_wait(smem_addr(&landed[g % kNS]), (g / kNS) & 1, nullptr);
-      if (warp == kProdWarp0 && q_issued > 0)
-        mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
+      if (bad_block) set_status(p.status, PKV_DEV_BAD_BLOCK);
+      // our copies, and the barrier arrivals they trigger, land before the CTA can exit
+      if (lane == 0) {
+        uint64_t* landed = vrole ? bars->v_landed : bars->k_full;
+        for (int g = max(0, armed - kNS); g < armed; ++g)
+          mbar_wait(smem_addr(&landed[g % kNS]), (g / kNS) & 1, nullptr);
+        if (!vrole && q_issued > 0)
+          mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
+      }
     }
   } else if (warp >= kMmaWarp) {
     setmaxnreg_dec<kOtherRegs>();
-    if (F16P && warp >= kConvWarp0) {
-      // ===== converters (fp16 P): each landed V stage to fp16 in place =====
+    if (warp >= kConvWarp0) {
+      // ===== converters: each landed V stage to fp16 in place =====
       // piece i of a stage (row i / RP, 16-byte column unit i % RP) is
-      // converted by thread i mod 96; the stage is then published to the
-      // tensor core's (async) proxy
+      // converted by thread i mod 96 (rows not loaded, or past the needed
+      // keys, are zeroed); the stage is then published to the tensor core's
+      // (async) proxy
       constexpr int RP = D / 8;
       const int ct = threadIdx.x - kConvWarp0 * 32;
       uint32_t emax = 0;  // V exponent fields seen (range check)
@@ -677,12 +668,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(kFullMask, w, 0) != 0;
           if (!ok) break;
           const uint32_t base = v_s + st * Lay::TILE_BYTES;
+          const uint32_t load = *reinterpret_cast<volatile uint32_t*>(&bars->v_mask[st]);
+          const int nvalid = d.kv_end - (d.jb + j) * kBN;  // rows below it are needed keys
 #pragma unroll 4
           for (int i = ct; i < kBN * RP; i += kConverters) {
             const int k = i / RP, pc = i % RP;
-            v_piece_to_f16(base + (pc >> 3) * Lay::CH_BYTES + k * 128 +
-                               (((uint32_t)(pc & 7) ^ (uint32_t)(k & 7)) << 4),
-                           emax);
+            const uint32_t a = base + (pc >> 3) * Lay::CH_BYTES + k * 128 +
+                               (((uint32_t)(pc & 7) ^ (uint32_t)(k & 7)) << 4);
+            if (k < nvalid && ((load >> (k / kSub)) & 1u))
+              v_piece_to_f16(a, emax);
+            else
+              st_shared_zero16(a);
           }
           fence_proxy_async_smem();
           mbar_arrive(smem_addr(&bars->v_full[st]));
@@ -695,8 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= MMA issuer (one thread of warp 12) =================
     if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv =
-          F16P ? umma_idesc_f16(kBM, D, false, true) : umma_idesc_bf16(kBM, D, false, true);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(kBM, D, false, true);
       bool ok = true;
       int gi = 0, gt = 0;
       // S_x = Q_x K_g^T (the K stage is released after the last Q tile's product)
@@ -721,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       static_assert(kNS == 2 && kQT == 2, "two-way selects below");
       auto issue_qk = [&](int x, int g) {
-        fence_proxy_async_smem();  // K was written by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t d_tmem = tmem + Lay::s_col(x);
         const uint64_t qd = x ? qdesc[1] : qdesc[0], kd = (g & 1) ? kdesc[1] : kdesc[0];
@@ -733,23 +727,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (x == kQT - 1) umma_commit((g & 1) ? k_empty_b[1] : k_empty_b[0]);
         umma_commit(x ? s_full_b[1] : s_full_b[0]);
       };
-      // O_x += P_x V_g (fp16 P and V; or bf16 high parts, then the remainders)
+      // O_x += P_x V_g (fp16 P and V; the converters fenced their V writes
+      // to the async proxy before publishing the stage)
       auto issue_pv = [&](int x, int g, bool first) {
-        fence_proxy_async_smem();  // V was written by cp.async / st.shared (generic proxy)
         tc_fence_after();
         const uint32_t s_base = tmem + Lay::s_col(x);
         const uint32_t o_base = tmem + Lay::o_col(x);
         const uint64_t vd = (g & 1) ? vdesc[1] : vdesc[0];
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(o_base, s_base + (F16P ? Lay::p_col(kk) : Lay::p_hi_col(kk)),
-                  vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        if (!F16P) {
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(o_base, s_base + Lay::p_hi_col(kk) + 16, vd + (uint32_t)((kk * 16 * 128) >> 4),
-                    idesc_pv, 1u);
-        }
+          umma_ts(o_base, s_base + Lay::p_col(kk), vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv,
+                  (!first || kk > 0) ? 1u : 0u);
         if (x == kQT - 1) umma_commit((g & 1) ? v_empty_b[1] : v_empty_b[0]);
         umma_commit(x ? o_done_b[1] : o_done_b[0]);
       };
@@ -769,11 +757,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = d.n_tiles;
         ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
         // S_x is reused after PV of the previous item's last tile: in issue order
+        // (the Q-tile loops stay rolled: one copy of the issue code keeps
+        // this thread's instruction footprint small)
+#pragma unroll 1
         for (int x = 0; ok && x < kQT; ++x) issue_qk(x, gt);
         if (!ok) break;
         if (n == 1) umma_commit(smem_addr(&bars->q_empty));  // Q of this item no longer read
         for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j;
+#pragma unroll 1
           for (int x = 0; ok && x < kQT; ++x) {
             // the first PV of an item overwrites O_x: the previous item's
             // epilogue must have read it
@@ -855,63 +847,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float2 sl2x2 = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
-          if constexpr (F16P) {
-            // pass 2: probabilities as fp16 pairs, written over the first half
-            // of the chunk's S columns; the row sum adds the rounded values,
-            // so that O and l see the same weights
-            float rsa = 0.f, rsb = 0.f;
+          // pass 2: probabilities as fp16 pairs, written over the first half
+          // of the chunk's S columns; the row sum adds the rounded values,
+          // so that O and l see the same weights
+          float rsa = 0.f, rsb = 0.f;
 #pragma unroll 1
-            for (int ch = 0; ch < kBN / 32; ++ch) {
-              uint32_t u[32];
-              PKV_TMEM_LD32(sa + ch * 32, u);
-              tmem_wait_ld();
-              uint32_t pk[16];
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t u[32];
+            PKV_TMEM_LD32(sa + ch * 32, u);
+            tmem_wait_ld();
+            uint32_t pk[16];
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float2 x2 = __ffma2_rn(
-                    make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
-                    negm);
-                pk[c] = pack_f16x2(fast_exp2(x2.x), fast_exp2(x2.y));
-                add_f16x2_to(rsa, rsb, pk[c]);
-              }
-              PKV_TMEM_ST16(sa + ch * 16, pk);
+            for (int c = 0; c < 16; ++c) {
+              const float2 x2 = __ffma2_rn(
+                  make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
+                  negm);
+              pk[c] = pack_f16x2(fast_exp2(x2.x), fast_exp2(x2.y));
+              add_f16x2_to(rsa, rsb, pk[c]);
             }
-            tmem_wait_st();
-            rs = rsa + rsb;
-          } else {
-            // pass 2: probabilities in place as packed bf16 hi | lo, where hi
-            // keeps the top 16 bits of p and lo = p - hi (exact) is truncated
-            // the same way: hi + lo is p to 2^-14 relative
-            const float2 minus1 = make_float2(-1.f, -1.f);
-            float2 rsa = make_float2(0.f, 0.f), rsb = make_float2(0.f, 0.f);
-#pragma unroll 1
-            for (int ch = 0; ch < kBN / 32; ++ch) {
-              uint32_t u[32];
-              PKV_TMEM_LD32(sa + ch * 32, u);
-              tmem_wait_ld();
-              uint32_t pk[32];
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float2 x2 = __ffma2_rn(
-                    make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
-                    negm);
-                const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
-                if (c & 1)
-                  rsb = __fadd2_rn(rsb, p2);
-                else
-                  rsa = __fadd2_rn(rsa, p2);
-                const uint32_t b0 = __float_as_uint(p2.x), b1 = __float_as_uint(p2.y);
-                const float2 hi2 = make_float2(__uint_as_float(b0 & 0xffff0000u),
-                                               __uint_as_float(b1 & 0xffff0000u));
-                const float2 lo2 = __ffma2_rn(hi2, minus1, p2);
-                pk[c] = __byte_perm(b0, b1, 0x7632);
-                pk[16 + c] = __byte_perm(__float_as_uint(lo2.x), __float_as_uint(lo2.y), 0x7632);
-              }
-              PKV_TMEM_ST32(sa + ch * 32, pk);
-            }
-            tmem_wait_st();
-            rs = (rsa.x + rsb.x) + (rsa.y + rsb.y);
+            PKV_TMEM_ST16(sa + ch * 16, pk);
           }
+          tmem_wait_st();
+          rs = rsa + rsb;
         } else {
           // ---- a diagonal tile: hide the keys after each row's position
           // pass 1: row maximum over the visible keys
@@ -939,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t u[32];
             PKV_TMEM_LD32(sa + ch * 32, u);
             tmem_wait_ld();
-            uint32_t pk[F16P ? 16 : 32];
+            uint32_t pk[16];
             const int vis = lim - ch * 32;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -947,19 +904,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -m));
               if (2 * c > vis) p0 = 0.f;
               if (2 * c + 1 > vis) p1 = 0.f;
-              if constexpr (F16P) {
-                pk[c] = pack_f16x2(p0, p1);
-                add_f16x2_to(rsa, rsb, pk[c]);
-              } else {
-                rsa += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-                pk[16 + c] = pack_bf16x2(p0 - bf16_lo(pk[c]), p1 - bf16_hi(pk[c]));
-              }
+              pk[c] = pack_f16x2(p0, p1);
+              add_f16x2_to(rsa, rsb, pk[c]);
             }
-            if constexpr (F16P)
-              PKV_TMEM_ST16(sa + ch * 16, pk);
-            else
-              PKV_TMEM_ST32(sa + ch * 32, pk);
+            PKV_TMEM_ST16(sa + ch * 16, pk);
           }
           tmem_wait_st();
           rs = rsa + rsb;
@@ -1040,17 +988,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) cta_finished(p);
 }
 
-#ifndef PKV_PREFILL_F16P
-#define PKV_PREFILL_F16P 1
-#endif
-
 template <int D>
-cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream,
-                             int priority) {
+cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
+                             const CUtensorMap& kv_map, cudaStream_t stream, int priority) {
   using Lay = PrefillLayout<D>;
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kernel = prefill_kernel<D, PKV_PREFILL_F16P != 0>;
+  auto kernel = prefill_kernel<D>;
   static SmemLimit limit;
   if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), 227 * 1024);
       e != cudaSuccess)
@@ -1075,15 +1019,15 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map, cuda
   attr[1].val.priority = priority;
   cfg.attrs = attr;
   cfg.numAttrs = priority != 0 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, q_map, p);
+  return cudaLaunchKernelEx(&cfg, kernel, q_map, kv_map, p);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map, cudaStream_t stream,
-                           int priority) {
-  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, stream, priority);
-  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, stream, priority);
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
+                           const CUtensorMap& kv_map, cudaStream_t stream, int priority) {
+  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, kv_map, stream, priority);
+  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, kv_map, stream, priority);
   return cudaErrorInvalidValue;
 }
 
