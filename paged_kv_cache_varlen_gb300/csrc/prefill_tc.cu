@@ -74,15 +74,19 @@ namespace {
 
 constexpr int kBM = 128;                             // Q rows per tile
 constexpr int kQT = 2;                               // Q tiles per work item
-constexpr int kBN = 128;                             // keys per KV tile
+constexpr int kBN = 128;                             // keys per K/V tile (one ring stage)
+constexpr int kSN = 64;                              // keys per S tile (half a K/V tile)
+constexpr int kSB = 2;                               // S buffers per Q tile
 constexpr int kNS = 2;                               // stages of each of the K and V rings
 constexpr int kSub = 16;                             // keys per TMA box
 constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 7 (warpgroups 0, 1)
-constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warp 8: Q and K tiles (warp 9 idle)
-constexpr int kVWarp0 = kProdWarp0 + 2;              // warp 10: V tiles (warp 11 idle)
-constexpr int kMmaWarp = kVWarp0 + 2;                // warp 12
-constexpr int kConvWarp0 = kMmaWarp + 1;             // warps 13-15: V to fp16 (fp16 P only)
-constexpr int kConverters = 3 * 32;
+constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warp 8: Q and K tiles
+constexpr int kVWarp0 = kProdWarp0 + 2;              // warp 10: V tiles
+constexpr int kMmaWarp = kVWarp0 + 2;                // warps 12, 13: MMA issue for Q tiles A, B
+constexpr int kConverters = 4 * 32;                  // warps 9, 11, 14, 15: V to fp16
+__device__ __forceinline__ int converter_slot(int warp) {
+  return warp == kProdWarp0 + 1 ? 0 : warp == kVWarp0 + 1 ? 1 : warp - kMmaWarp;
+}
 constexpr int kThreads = 512;                        // four warpgroups
 // registers per thread: launched with 128; the softmax warpgroups take 152,
 // the producer / MMA warpgroups give theirs down to 104 (2*152 + 2*104 = 4*128)
@@ -92,9 +96,9 @@ static_assert(2 * kSoftmaxRegs + 2 * kOtherRegs == 4 * (65536 / kThreads),
               "the register split adds up to the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRing = 4;  // work items announced ahead of the roles that consume them
-// readers of an announced item: the V producer warp, the MMA thread, the
-// eight softmax warps and the three converter warps (one lane each)
-constexpr int kItemReaders = 1 + 1 + kSoftmaxThreads / 32 + 3;
+// readers of an announced item: the V producer warp, the two MMA threads,
+// the eight softmax warps and the four converter warps (one lane each)
+constexpr int kItemReaders = 1 + kQT + kSoftmaxThreads / 32 + kConverters / 32;
 constexpr float kRescaleThreshold = 8.f;
 constexpr uint32_t kFullMask = 0xffffffffu;
 
@@ -126,20 +130,23 @@ struct PrefillLayout {
     const size_t need = 1024 + PREF_OFF + work_list_ints(num_seqs) * 4;
     return need > 120 * 1024 ? need : 120 * 1024;
   }
-  // TMEM columns: S of tile x (P written in place), then O of tile x
-  __device__ static constexpr uint32_t s_col(int x) { return 128u * (uint32_t)x; }
-  __device__ static constexpr uint32_t o_col(int x) { return 128u * (uint32_t)(kQT + x); }
+  // TMEM columns of Q tile x: its two S buffers of kSN columns (P written
+  // in place), then O
+  __device__ static constexpr uint32_t s_col(int x, int b) {
+    return 256u * (uint32_t)x + (uint32_t)(b * kSN);
+  }
+  __device__ static constexpr uint32_t o_col(int x) { return 256u * (uint32_t)x + 128u; }
   // P of keys 16*kk .. 16*kk+15 inside an S buffer: fp16 pairs in 8 columns
   __device__ static constexpr uint32_t p_col(int kk) { return 8u * (uint32_t)kk; }
 };
-static_assert(kQT * 2 * 128 <= (int)kTmemCols, "S and O of every Q tile fit in TMEM");
+static_assert(kQT * (kSB * kSN + 128) <= (int)kTmemCols, "S and O of every Q tile fit in TMEM");
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kNS], k_empty[kNS];
   uint64_t v_full[kNS], v_empty[kNS];
   uint64_t v_landed[kNS];  // V copies arrived (bf16), not yet converted
-  uint64_t s_full[kQT];   // QK^T of the tile landed in S_x
+  uint64_t s_full[kQT][kSB];  // QK^T of the S tile landed in buffer b of S_x
   uint64_t p_ready[kQT];  // the warpgroup stored P_x (and rescaled O_x)
   uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
   uint64_t o_free[kQT];   // the warpgroup's epilogue has read O_x
@@ -154,6 +161,7 @@ struct Bars {
 
 struct PrefillItem {
   int req, kvh, j0, j1, t0, qlen, L, kv_end, n_tiles;
+  int n_sub;  // S tiles of kSN keys: the needed keys of the n_tiles K/V tiles (at least 1)
   int qpos0;  // position of the request's first query among its keys
   int jb;   // first key tile of the item (a key segment in prefix mode)
   int seg;  // key segment (prefix mode), else 0
@@ -353,6 +361,7 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const W
     d.kv_end = d.L;  // every query sees the whole prefix
     d.jb = d.seg * tps;
     d.n_tiles = min((d.L + kBN - 1) / kBN, d.jb + tps) - d.jb;
+    d.n_sub = max(1, (min(d.L, (d.jb + d.n_tiles) * kBN) - d.jb * kBN + kSN - 1) / kSN);
     return d;
   }
   const int qt = ntq - 1 - local;  // later (heavier) units first
@@ -366,6 +375,7 @@ __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const W
   // key is visible) so that the item's rows are written
   d.kv_end = max(0, min(d.L, d.qpos0 + d.j1));
   d.n_tiles = max(1, (d.kv_end + kBN - 1) / kBN);
+  d.n_sub = max(1, (d.kv_end + kSN - 1) / kSN);
   d.jb = 0;
   d.seg = 0;
   return d;
@@ -485,21 +495,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup: barriers (first producer warp), work list (all), TMEM (MMA warp)
   if (warp == kProdWarp0 && lane == 0) {
     mbar_init(smem_addr(&bars->q_full), 1);
-    mbar_init(smem_addr(&bars->q_empty), 1);
+    mbar_init(smem_addr(&bars->q_empty), kQT);  // one commit per MMA thread
     for (int s = 0; s < kNS; ++s) {
       mbar_init(smem_addr(&bars->k_full[s]), 1);  // the producer's arrival + TMA bytes
-      mbar_init(smem_addr(&bars->k_empty[s]), 1);
+      mbar_init(smem_addr(&bars->k_empty[s]), kQT);
       mbar_init(smem_addr(&bars->v_full[s]), kConverters);
-      mbar_init(smem_addr(&bars->v_empty[s]), 1);
+      mbar_init(smem_addr(&bars->v_empty[s]), kQT);
       mbar_init(smem_addr(&bars->v_landed[s]), 1);
     }
     for (int x = 0; x < kQT; ++x) {
-      mbar_init(smem_addr(&bars->s_full[x]), 1);
+      for (int b = 0; b < kSB; ++b) mbar_init(smem_addr(&bars->s_full[x][b]), 1);
       mbar_init(smem_addr(&bars->p_ready[x]), kBM / 32);  // one arrival per softmax warp
       mbar_init(smem_addr(&bars->o_done[x]), 1);
       mbar_init(smem_addr(&bars->o_free[x]), kBM / 32);
     }
-    mbar_init(smem_addr(&bars->mma_done), 1);
+    mbar_init(smem_addr(&bars->mma_done), kQT);
     for (int k = 0; k < kRing; ++k) {
       mbar_init(smem_addr(&bars->item_full[k]), 1);
       mbar_init(smem_addr(&bars->item_empty[k]), kItemReaders);
@@ -532,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // control-flow merge between the change and the code that relies on it):
   // warpgroup 2 (producers) and 3 (MMA + idle warps) give registers back,
   // warpgroups 0 and 1 (softmax) take them.
-  if (warp >= kProdWarp0 && warp < kMmaWarp) {
+  if (warp >= kProdWarp0) {
     setmaxnreg_dec<kOtherRegs>();
-    // ===== producers: Q (warp 8) and the K tiles (warp 8), the V tiles (warp
-    // 10), all by TMA; warps 9 and 11 have no work =====
+    // ===== producers: Q and the K tiles (warp 8), the V tiles (warp 10),
+    // all by TMA =====
     // A 128-key tile is 8 boxes of 16 keys (a 16-key run never crosses a
     // page: block_size is a multiple of 16), each box one TMA copy per
     // 64-column chunk, landing 128-byte-swizzled in the layout the MMA
@@ -640,17 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!vrole && q_issued > 0)
           mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
       }
-    }
-  } else if (warp >= kMmaWarp) {
-    setmaxnreg_dec<kOtherRegs>();
-    if (warp >= kConvWarp0) {
-      // ===== converters: each landed V stage to fp16 in place =====
+    } else if (warp != kMmaWarp && warp != kMmaWarp + 1) {
+      // ===== converters (warps 9, 11, 14, 15): each landed V stage to fp16
+      // in place =====
       // piece i of a stage (row i / RP, 16-byte column unit i % RP) is
-      // converted by thread i mod 96 (rows not loaded, or past the needed
-      // keys, are zeroed); the stage is then published to the tensor core's
-      // (async) proxy
+      // converted by converter thread i mod 128 (rows not loaded, or past
+      // the needed keys, are zeroed); the stage is then published to the
+      // tensor core's (async) proxy
       constexpr int RP = D / 8;
-      const int ct = threadIdx.x - kConvWarp0 * 32;
+      const int ct = converter_slot(warp) * 32 + lane;
       uint32_t emax = 0;  // V exponent fields seen (range check)
       int gt = 0;
       bool ok = true;
@@ -687,26 +695,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a bf16 exponent field >= 143 is a magnitude >= 2^16 (or inf / NaN)
       if ((emax & 0xffffu) >= 0x4780u || (emax >> 16) >= 0x4780u)
         set_status(p.status, PKV_DEV_V_RANGE);
-    }
-    // ================= MMA issuer (one thread of warp 12) =================
-    if (warp == kMmaWarp && lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false, false);
+    } else if (lane == 0) {
+      // ============ MMA issuers: one thread of warp 12 for Q tile A, one of
+      // warp 13 for Q tile B ============
+      // Each issues its own tile's products in order over S tiles of kSN
+      // keys (the halves of the K/V tiles): QK(0) and QK(1) into the two S
+      // buffers, then for every S tile j: PV(j), QK(j+2). S tile j+1 is
+      // thus computed while the softmax works on j, and the softmax
+      // warpgroup goes from one tile to the next without waiting for the
+      // tensor core. A buffer holds P(j) until PV(j) has read it; tcgen05
+      // operations of one thread run in issue order, so QK(j+2) into the
+      // same buffer may follow PV(j) at once. The two threads' MMAs
+      // interleave on the tensor core. A K or V stage is released when both
+      // threads' products that read it are done (two commits); so is Q.
+      // Descriptors and barrier addresses are computed once; an operand
+      // offset only adds to the start-address field (16-byte units).
+      const int x = warp - kMmaWarp;
+      constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kSN, false, false);
       constexpr uint32_t idesc_pv = umma_idesc_f16(kBM, D, false, true);
-      bool ok = true;
-      int gi = 0, gt = 0;
-      // S_x = Q_x K_g^T (the K stage is released after the last Q tile's product)
-      // The thread shares its SM sub-partition with busy softmax warps, so
-      // its instructions per MMA are kept few: descriptors and barrier
-      // addresses are computed once; a k-step only adds its offset (in
-      // 16-byte units) to the start-address field.
-      uint64_t qdesc[kQT], kdesc[kNS], vdesc[kNS];
-      uint32_t k_empty_b[kNS], v_empty_b[kNS], s_full_b[kQT], o_done_b[kQT];
-#pragma unroll
-      for (int x = 0; x < kQT; ++x) {
-        qdesc[x] = smem_desc_sw128(q_s + x * Lay::TILE_BYTES, 16, 1024);
-        s_full_b[x] = smem_addr(&bars->s_full[x]);
-        o_done_b[x] = smem_addr(&bars->o_done[x]);
-      }
+      const uint64_t qd = smem_desc_sw128(q_s + x * Lay::TILE_BYTES, 16, 1024);
+      uint64_t kdesc[kNS], vdesc[kNS];
+      uint32_t k_empty_b[kNS], v_empty_b[kNS];
 #pragma unroll
       for (int st = 0; st < kNS; ++st) {
         kdesc[st] = smem_desc_sw128(k_s + st * Lay::TILE_BYTES, 16, 1024);
@@ -714,80 +723,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         k_empty_b[st] = smem_addr(&bars->k_empty[st]);
         v_empty_b[st] = smem_addr(&bars->v_empty[st]);
       }
-      static_assert(kNS == 2 && kQT == 2, "two-way selects below");
-      auto issue_qk = [&](int x, int g) {
+      static_assert(kNS == 2 && kSB == 2 && kBN == 2 * kSN, "two-way selects below");
+      const uint32_t s_full_b[kSB] = {smem_addr(&bars->s_full[x][0]),
+                                      smem_addr(&bars->s_full[x][1])};
+      const uint32_t o_done_b = smem_addr(&bars->o_done[x]);
+      const uint32_t s_tmem = tmem + Lay::s_col(x, 0);
+      const uint32_t o_tmem = tmem + Lay::o_col(x);
+      constexpr uint32_t kHalf16 = (kSN * 128) >> 4;  // rows of half a K/V tile, in 16-byte units
+      // S(g) = Q_x K^T over half h of K/V tile kt; `rel`: the last S tile
+      // that reads the K stage
+      auto issue_qk = [&](int g, int kt, int h, bool rel) {
         tc_fence_after();
-        const uint32_t d_tmem = tmem + Lay::s_col(x);
-        const uint64_t qd = x ? qdesc[1] : qdesc[0], kd = (g & 1) ? kdesc[1] : kdesc[0];
+        const uint32_t d_tmem = s_tmem + (uint32_t)((g & 1) * kSN);
+        const uint64_t kd = ((kt & 1) ? kdesc[1] : kdesc[0]) + (h ? kHalf16 : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off16 = ((kk >> 2) * Lay::CH_BYTES + (kk & 3) * 32) >> 4;
           umma_ss(d_tmem, qd + off16, kd + off16, idesc_qk, kk > 0);
         }
-        if (x == kQT - 1) umma_commit((g & 1) ? k_empty_b[1] : k_empty_b[0]);
-        umma_commit(x ? s_full_b[1] : s_full_b[0]);
+        if (rel) umma_commit((kt & 1) ? k_empty_b[1] : k_empty_b[0]);
+        umma_commit((g & 1) ? s_full_b[1] : s_full_b[0]);
       };
-      // O_x += P_x V_g (fp16 P and V; the converters fenced their V writes
-      // to the async proxy before publishing the stage)
-      auto issue_pv = [&](int x, int g, bool first) {
+      // O_x += P(g) V over half h of K/V tile kt (fp16 P and V; the
+      // converters fenced their V writes to the async proxy before
+      // publishing the stage)
+      auto issue_pv = [&](int g, int kt, int h, bool first, bool rel) {
         tc_fence_after();
-        const uint32_t s_base = tmem + Lay::s_col(x);
-        const uint32_t o_base = tmem + Lay::o_col(x);
-        const uint64_t vd = (g & 1) ? vdesc[1] : vdesc[0];
+        const uint32_t p_tmem = s_tmem + (uint32_t)((g & 1) * kSN);
+        const uint64_t vd = ((kt & 1) ? vdesc[1] : vdesc[0]) + (h ? kHalf16 : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(o_base, s_base + Lay::p_col(kk), vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv,
+        for (int kk = 0; kk < kSN / 16; ++kk)
+          umma_ts(o_tmem, p_tmem + Lay::p_col(kk), vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv,
                   (!first || kk > 0) ? 1u : 0u);
-        if (x == kQT - 1) umma_commit((g & 1) ? v_empty_b[1] : v_empty_b[0]);
-        umma_commit(x ? o_done_b[1] : o_done_b[0]);
+        if (rel) umma_commit((kt & 1) ? v_empty_b[1] : v_empty_b[0]);
+        umma_commit(o_done_b);
       };
-      // Fixed issue order per item: QK_A(0), QK_B(0), then for every tile j
-      // PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1). After the first tile this
-      // puts the two warpgroups half a period apart: the softmax of one Q
-      // tile runs while the tensor core works through the other tile's PV
-      // and next QK^T, instead of both softmaxes running at once and the
-      // tensor core idling meanwhile.
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return mbar_wait(smem_addr(bar), parity, p.status, abort);
       };
+      bool ok = true;
+      int gi = 0, gt = 0, gs = 0;  // items, K/V tiles, S tiles so far
       for (; ok; ++gi) {
         const int it = read_item(bars, p, gi, abort);
         if (it < 0) break;
         const PrefillItem d = prefill_item(p, wl, QP, it);
-        const int n = d.n_tiles;
+        const int ns = d.n_sub;
+        // both S buffers are free: the previous item's PVs were issued first
         ok = wait(&bars->q_full, gi & 1) && wait(&bars->k_full[gt % kNS], (gt / kNS) & 1);
-        // S_x is reused after PV of the previous item's last tile: in issue order
-        // (the Q-tile loops stay rolled: one copy of the issue code keeps
-        // this thread's instruction footprint small)
-#pragma unroll 1
-        for (int x = 0; ok && x < kQT; ++x) issue_qk(x, gt);
         if (!ok) break;
-        if (n == 1) umma_commit(smem_addr(&bars->q_empty));  // Q of this item no longer read
-        for (int j = 0; ok && j < n; ++j) {
-          const int g = gt + j;
-#pragma unroll 1
-          for (int x = 0; ok && x < kQT; ++x) {
-            // the first PV of an item overwrites O_x: the previous item's
-            // epilogue must have read it
-            ok = wait(&bars->p_ready[x], g & 1) &&
-                 wait(&bars->v_full[g % kNS], (g / kNS) & 1) &&
-                 (j > 0 || gi == 0 || wait(&bars->o_free[x], (gi - 1) & 1));
+        issue_qk(gs, gt, 0, ns == 1);
+        if (ns > 1) issue_qk(gs + 1, gt, 1, true);
+        if (ns <= 2) umma_commit(smem_addr(&bars->q_empty));  // Q of this item no longer read
+        for (int j = 0; ok && j < ns; ++j) {
+          const int g = gs + j, kt = gt + (j >> 1), h = j & 1;
+          // the first PV of an item overwrites O_x: the previous item's
+          // epilogue must have read it
+          ok = wait(&bars->p_ready[x], g & 1) &&
+               (h || wait(&bars->v_full[kt % kNS], (kt / kNS) & 1)) &&
+               (j > 0 || gi == 0 || wait(&bars->o_free[x], (gi - 1) & 1));
+          if (!ok) break;
+          issue_pv(g, kt, h, j == 0, h || j == ns - 1);
+          if (j + 2 < ns) {
+            const int kt2 = gt + ((j + 2) >> 1);
+            ok = h || wait(&bars->k_full[kt2 % kNS], (kt2 / kNS) & 1);
             if (!ok) break;
-            issue_pv(x, g, j == 0);
-            if (j + 1 < n) {
-              // S_x holds P_x(j) until this PV has read it: tcgen05.mma
-              // operations issued by one thread run in issue order, so the
-              // next QK^T into S_x may follow the PV at once
-              ok = wait(&bars->k_full[(g + 1) % kNS], ((g + 1) / kNS) & 1);
-              if (!ok) break;
-              issue_qk(x, g + 1);
-              if (x == kQT - 1 && j + 2 == n) umma_commit(smem_addr(&bars->q_empty));
-            }
+            issue_qk(g + 2, kt2, h, h || j + 2 == ns - 1);
+            if (j + 2 == ns - 1) umma_commit(smem_addr(&bars->q_empty));
           }
         }
-        gt += n;
+        gt += d.n_tiles;
+        gs += ns;
       }
-      // every MMA issued so far has completed before TMEM is released
+      // every MMA issued so far (by both threads) has completed before TMEM
+      // is released
       umma_commit(smem_addr(&bars->mma_done));
       mbar_wait(smem_addr(&bars->mma_done), 0, nullptr);
     }
@@ -799,11 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rq = r / G;  // query of the row inside its tile
     const int g = r % G;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t sa = tmem + lane_base + Lay::s_col(x);
+    const uint32_t sa0 = tmem + lane_base + Lay::s_col(x, 0);
     const uint32_t oa = tmem + lane_base + Lay::o_col(x);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int gt = 0;
+    int gs = 0;  // S tiles of this Q tile so far (all items)
     for (int k = 0; ok; ++k) {
       int it = -1;
       if (lane == 0) it = read_item(bars, p, k, abort);
@@ -816,28 +824,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos =
           (row_valid && !p.prefix_mode) ? min(d.qpos0 + qj, d.kv_end - 1) : (d.kv_end - 1);
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < d.n_tiles; ++j) {
-        const int gg = gt + j;
-        ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->s_full[x]), gg & 1, p.status, abort));
+      for (int j = 0; j < d.n_sub; ++j) {
+        const int gg = gs + j;
+        const uint32_t sa = sa0 + (uint32_t)((gg & 1) * kSN);
+        ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->s_full[x][gg & 1]), (gg >> 1) & 1,
+                                             p.status, abort));
         if (!ok) break;
         tc_fence_after();
-        const int lim = pos - (d.jb + j) * kBN;  // keys c <= lim of this tile are visible
-        float alpha = 1.f, rs;
+        const int lim = pos - (d.jb * kBN + j * kSN);  // keys c <= lim of this tile are visible
+        // the row's kSN scores in registers: one TMEM round trip
+        uint32_t u[kSN];
+        PKV_TMEM_LD32(sa, u);
+        PKV_TMEM_LD32(sa + 32, (u + 32));
+        tmem_wait_ld();
+        float alpha = 1.f, rsa = 0.f, rsb = 0.f;
         bool resc;
-        if (__all_sync(kFullMask, lim >= kBN - 1)) {
-          // ---- every key of the tile is visible to every row of the warp
-          // pass 1: row maximum (two independent chains of 3-input maxima)
+        if (__all_sync(kFullMask, lim >= kSN - 1)) {
+          // ---- every key of the tile is visible to every row of the warp:
+          // row maximum (two independent chains of 3-input maxima), then the
+          // probabilities as fp16 pairs, written over the first half of the
+          // S columns; the row sum adds the rounded values, so that O and l
+          // see the same weights
           float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t u[32];
-            PKV_TMEM_LD32(sa + ch * 32, u);
-            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 16; c += 2) {
-              mxa = max3(mxa, __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
-              mxb = max3(mxb, __uint_as_float(u[2 * c + 2]), __uint_as_float(u[2 * c + 3]));
-            }
+          for (int c = 0; c < kSN / 2; c += 2) {
+            mxa = max3(mxa, __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
+            mxb = max3(mxb, __uint_as_float(u[2 * c + 2]), __uint_as_float(u[2 * c + 3]));
           }
           const float mnew = fmaxf(m, fmaxf(mxa, mxb) * sl2);
           resc = mnew > m + kRescaleThreshold;
@@ -847,74 +859,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float2 sl2x2 = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
-          // pass 2: probabilities as fp16 pairs, written over the first half
-          // of the chunk's S columns; the row sum adds the rounded values,
-          // so that O and l see the same weights
-          float rsa = 0.f, rsb = 0.f;
-#pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t u[32];
-            PKV_TMEM_LD32(sa + ch * 32, u);
-            tmem_wait_ld();
+#pragma unroll
+          for (int ch = 0; ch < kSN / 32; ++ch) {
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float2 x2 = __ffma2_rn(
-                  make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2x2,
-                  negm);
+              const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(u[32 * ch + 2 * c]),
+                                                       __uint_as_float(u[32 * ch + 2 * c + 1])),
+                                           sl2x2, negm);
               pk[c] = pack_f16x2(fast_exp2(x2.x), fast_exp2(x2.y));
               add_f16x2_to(rsa, rsb, pk[c]);
             }
             PKV_TMEM_ST16(sa + ch * 16, pk);
           }
-          tmem_wait_st();
-          rs = rsa + rsb;
         } else {
           // ---- a diagonal tile: hide the keys after each row's position
-          // pass 1: row maximum over the visible keys
           float mx = -INFINITY;
-#pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t u[32];
-            PKV_TMEM_LD32(sa + ch * 32, u);
-            tmem_wait_ld();
-            const int vis = lim - ch * 32;
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c <= vis) mx = fmaxf(mx, __uint_as_float(u[c]));
-          }
+          for (int c = 0; c < kSN; ++c)
+            if (c <= lim) mx = fmaxf(mx, __uint_as_float(u[c]));
           const float mnew = fmaxf(m, mx * sl2);
           resc = mnew > m + kRescaleThreshold;
           if (resc) {
             alpha = fast_exp2(m - mnew);  // 0 on the first tile
             m = mnew;
           }
-          // pass 2: probabilities, stored as fp16 pairs (or bf16 hi | lo)
-          float rsa = 0.f, rsb = 0.f;
-#pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t u[32];
-            PKV_TMEM_LD32(sa + ch * 32, u);
-            tmem_wait_ld();
+#pragma unroll
+          for (int ch = 0; ch < kSN / 32; ++ch) {
             uint32_t pk[16];
-            const int vis = lim - ch * 32;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * c]), sl2, -m));
-              float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -m));
-              if (2 * c > vis) p0 = 0.f;
-              if (2 * c + 1 > vis) p1 = 0.f;
+              const int c0 = 32 * ch + 2 * c;
+              float p0 = fast_exp2(fmaf(__uint_as_float(u[c0]), sl2, -m));
+              float p1 = fast_exp2(fmaf(__uint_as_float(u[c0 + 1]), sl2, -m));
+              if (c0 > lim) p0 = 0.f;
+              if (c0 + 1 > lim) p1 = 0.f;
               pk[c] = pack_f16x2(p0, p1);
               add_f16x2_to(rsa, rsb, pk[c]);
             }
             PKV_TMEM_ST16(sa + ch * 16, pk);
           }
-          tmem_wait_st();
-          rs = rsa + rsb;
         }
-        l = l * alpha + rs;
+        tmem_wait_st();
+        l = l * alpha + (rsa + rsb);
         if (gg > 0) {
-          // the previous tile's PV has finished writing O_x
+          // the previous tile's PV has finished writing O_x (also keeps this
+          // warp within one phase of the o_done barrier)
           ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), (gg - 1) & 1,
                                                p.status, abort));
           if (!ok) break;
@@ -922,12 +912,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0 && __any_sync(kFullMask, resc)) {
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
-              uint32_t u[32];
-              PKV_TMEM_LD32(oa + 32 * c, u);
+              uint32_t v[32];
+              PKV_TMEM_LD32(oa + 32 * c, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-              PKV_TMEM_ST32(oa + 32 * c, u);
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              PKV_TMEM_ST32(oa + 32 * c, v);
             }
             tmem_wait_st();
           }
@@ -941,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue of the item: O / l -> out, lse
-      const int last = gt + d.n_tiles - 1;
+      const int last = gs + d.n_sub - 1;
       ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), last & 1, p.status,
                                            abort));
       if (!ok) break;
@@ -968,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&bars->o_free[x]));  // the MMA may overwrite O_x now
-      gt += d.n_tiles;
+      gs += d.n_sub;
     }
   }
 
