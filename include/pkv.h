@@ -15,11 +15,9 @@
  * - All tensor pointers are DEVICE pointers owned by the caller. The library
  *   never allocates device memory, never frees it, never synchronises the
  *   stream and keeps no state between calls, with stated exceptions: the
- *   built-in scratch array of pkv_paged_attention_varlen_noalloc, the
+ *   built-in scratch array of pkv_paged_attention_varlen_noalloc and the
  *   host-side block manager objects (pkv_bm_*), which the caller creates and
- *   destroys, and one side stream with two events per device and host
- *   thread that the attention calls create on first use (see
- *   pkv_paged_attention_varlen).
+ *   destroys.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream). A call returns as soon as the
  *   kernels are queued.
@@ -38,7 +36,7 @@
  *       kv_pool [2][num_blocks][block_size][num_kv_heads][head_dim] bf16,
  *       index 0 holds K, index 1 holds V; the pointer must be 16-byte aligned.
  *   Supported: head_dim 64 or 128; block_size a multiple of 16 (up to 256);
- *   num_heads a multiple of num_kv_heads.
+ *   num_heads a multiple of num_kv_heads; at most 65534 requests per call.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -158,12 +156,15 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
  * The kernels use programmatic dependent launch: each waits for the grid
  * before it in the stream to finish before touching memory, so ordinary
  * stream order holds. A batch with requests for both kernels runs them side
- * by side: the prefill grid on `stream` (at the device's highest launch
- * priority), the decode grids on a low-priority side stream that the library
- * creates once per device and host thread (with two events), forked from
- * `stream` at the start of the call and joined back into it at the end, so
- * the call is still ordered in `stream` as a whole (and records into a CUDA
- * graph as a fork and a join).
+ * by side, all on `stream`: the prefill grid first, keeping about its share
+ * of the SMs (prefill tiles against decode bytes, estimated on the device)
+ * and leaving the rest, then the decode grid, which launches once every
+ * prefill CTA has started and completes only after the prefill grid has.
+ * When num_tokens and max_query_len show that no request can be short
+ * enough for the decode kernel (num_seqs * max_query_len - num_tokens <
+ * max_query_len - max(1, 32 / G)), no decode grid is launched, and a
+ * request that is short anyway (cu_seqlens_q at odds with num_tokens) is
+ * flagged PKV_DEV_BAD_LENGTHS.
  */
 pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
                                       const void *kv_pool, const int32_t *block_table,
@@ -295,10 +296,10 @@ pkv_status pkv_paged_attention_varlen_noalloc(
  *            pkv_paged_attention_varlen); one workspace per concurrent call.
  * A request's context is its group's prefix followed by its tail. The prefix
  * pass runs every group's queries (members x heads as the rows of tensor-core
- * tiles) against the prefix blocks once, split into key segments; the tails
- * run through the decode kernel at the same time (on the side stream of
- * pkv_paged_attention_varlen, joined back before the merge); the partial
- * results merge by log-sum-exp.
+ * tiles) against the prefix blocks once, split into key segments, on about a
+ * quarter of the SMs; the tails run through the decode kernel at the same
+ * time on the others (launched right behind the prefix pass on `stream`);
+ * the partial results merge by log-sum-exp.
  * Errors: as pkv_paged_attention_varlen; PKV_DEV_BAD_LENGTHS for inconsistent
  * group_starts or lengths.
  */

@@ -3,8 +3,7 @@
 //
 // Nothing here allocates device memory, synchronises a stream or keeps
 // state across calls (the cached items are the driver entry point of
-// cuTensorMapEncodeTiled, per device the kernels' shared-memory limits, and
-// per device and host thread one side stream with two events).
+// cuTensorMapEncodeTiled and, per device, the kernels' shared-memory limits).
 // Every host-side check and tensor-map encoding of a call happens before its
 // first launch, so a rejected call enqueues nothing.
 #include <cuda.h>
@@ -190,6 +189,7 @@ pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q
     return PKV_OK;
   }
   if (num_seqs == 0) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65534) return PKV_ERR_UNSUPPORTED;  // grid z: requests + one
   if (!out || !q || !kv_pool || !block_table || !cu_seqlens_q || !seq_lens)
     return PKV_ERR_INVALID_ARG;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
@@ -306,68 +306,42 @@ pkv_status bind_workspace(AttnPlan* a, void* workspace, size_t workspace_bytes) 
   return PKV_OK;
 }
 
-// A side stream at the device's lowest priority and two events per device
-// and host thread, created on first use and kept until the process exits:
-// they let one call run its prefill and decode grids side by side (fork /
-// join inside the call).
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  int greatest_priority = 0;
-};
-
-cudaError_t side_stream(SideStream** out) {
-  constexpr int kMaxDevices = 64;
-  thread_local SideStream per_device[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  SideStream& ss = per_device[dev];
-  if (!ss.join) {
-    int least = 0, greatest = 0;
-    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
-    ss.greatest_priority = greatest;
-    if (!ss.stream &&
-        (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, least)) !=
-            cudaSuccess)
-      return e;
-    if (!ss.fork && (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) !=
-                        cudaSuccess)
-      return e;
-    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
-      return e;
-  }
-  *out = &ss;
-  return cudaSuccess;
+// Whether some request may be short enough for the decode kernel: with
+// every request at most max_query_len queries long and num_tokens in all,
+// n_short requests of at most decode_max_q queries need
+// n_short * (max_query_len - decode_max_q) <= num_seqs * max_query_len - num_tokens.
+bool may_have_decode(const AttnParams& p) {
+  return (int64_t)p.num_seqs * p.max_query_len - p.num_tokens >=
+         (int64_t)p.max_query_len - p.decode_max_q;
 }
 
-// Enqueue a planned call: the decode grid (and its split-KV merge grid), and
-// the prefill grid when some request is longer than the decode kernel takes.
-// With both, and `fork` set, the two run side by side: the prefill grid on
-// the caller's stream at the device's highest launch priority (so that its
-// one-CTA-per-SM persistent grid takes the SMs first), the decode grids on
-// the low-priority side stream behind an event recorded before it, their
-// CTAs filling the SMs that the prefill's last work items leave idle; the
-// caller's stream then waits for the side stream, so the call still
-// completes only when every grid has. Otherwise the grids run one after the
-// other on the caller's stream.
-pkv_status launch_plan(const AttnPlan& a, cudaStream_t st, bool fork = true) {
-  if (a.prefill && fork) {
-    SideStream* ss = nullptr;
-    if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(a.p, a.q_map, a.kv_box, st, ss->greatest_priority) != cudaSuccess)
+// Enqueue a planned call, all on the caller's stream: the decode grid (and
+// its split-KV merge grid) when no request is longer than the decode kernel
+// takes; otherwise the prefill grid, then -- unless no request can be short
+// -- the decode grid right behind it (programmatic dependent launch). The
+// prefill grid keeps its share of the SMs and leaves the rest to the decode
+// grid, which launches as soon as every prefill CTA has started or left;
+// the decode grid completes only after the prefill grid has (see
+// AttnParams::after_prefill), so the call completes when every grid has.
+pkv_status launch_plan(const AttnPlan& a, cudaStream_t st) {
+  if (!a.prefill)
+    return pkv::launch_decode_mma(a.p, a.kv_rows, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  AttnParams pp = a.p;
+  const bool decode = may_have_decode(a.p);
+  if (decode) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return PKV_ERR_CUDA;
-    if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pkv::launch_decode_mma(a.p, a.kv_rows, ss->stream) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess) return PKV_ERR_CUDA;
-    return cudaStreamWaitEvent(st, ss->join, 0) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    pp.shared_sms = sms;
+  } else {
+    pp.no_decode = 1;
   }
-  if (pkv::launch_decode_mma(a.p, a.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
-  if (a.prefill && pkv::launch_prefill(a.p, a.q_map, a.kv_box, st) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  return PKV_OK;
+  if (pkv::launch_prefill(pp, a.q_map, a.kv_box, st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (!decode) return PKV_OK;
+  AttnParams d = a.p;
+  d.after_prefill = 1;
+  return pkv::launch_decode_mma(d, a.kv_rows, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -397,8 +371,7 @@ pkv_status attention_with_scratch(float* out, float* out_lse, const void* q, con
   // the work tickets must start at zero (an interrupted earlier call may
   // have left them otherwise)
   if (cudaMemsetAsync(a.p.sched, 0, kSchedBytes, st) != cudaSuccess) return PKV_ERR_CUDA;
-  // one stream only: a side stream would be a resource created on first use
-  return launch_plan(a, st, false);
+  return launch_plan(a, st);
 }
 
 }  // namespace pkv
@@ -610,19 +583,14 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
       cudaSuccess)
     return PKV_ERR_CUDA;
   if (prefixes) {
-    // 2 + 3. the prefix pass (tensor cores, on `st` at the highest launch
-    // priority) and the tails (decode kernel, on the side stream) run side
-    // by side; they write disjoint partial slots
-    SideStream* ss = nullptr;
-    if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaEventRecord(ss->fork, st) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pkv::launch_prefill(p, q_map, kv_box, st, ss->greatest_priority) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    if (cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
-    if ((s = launch_plan(tails, ss->stream)) != PKV_OK) return s;
-    if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
-        cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    // 2 + 3. the prefix pass (tensor cores; its grid sized for about a
+    // quarter of the SMs), then right behind it the tails (decode kernel)
+    // on the SMs it leaves; they write disjoint partial slots, and the tail
+    // grid completes only after the prefix pass has
+    if (pkv::launch_prefill(p, q_map, kv_box, st) != cudaSuccess) return PKV_ERR_CUDA;
+    AttnParams d = tails.p;
+    d.after_prefill = 1;
+    if (pkv::launch_decode_mma(d, tails.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
   } else if ((s = launch_plan(tails, st)) != PKV_OK) {  // 2. tails only
     return s;
   }

@@ -112,9 +112,21 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   uint8_t* slots = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * SPW * SLOT);
 
-  // Everything below may read the pool the preceding KV write produces.
-  griddep_wait();
-  griddep_launch_dependents();
+  if (p.after_prefill) {
+    // Launched behind a prefill grid, which does not produce anything read
+    // here (it started after the preceding KV write had completed): only
+    // the extra CTA (z = num_seqs) waits for that grid to complete, so
+    // that this grid's completion implies the prefill grid's. The grid that
+    // follows launches when every CTA here has finished.
+    if ((int)blockIdx.z >= p.num_seqs) {
+      if (blockIdx.x == 0 && blockIdx.y == 0) griddep_wait();
+      return;
+    }
+  } else {
+    // Everything below may read the pool the preceding KV write produces.
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -570,7 +582,7 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
     return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_kv_heads * ((p.decode_max_rows + kRows - 1) / kRows), p.num_parts,
-                     p.num_seqs);
+                     p.num_seqs + (p.after_prefill ? 1 : 0));
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -84,6 +84,23 @@ struct AttnParams {
   int32_t prefix_mode;        // 0: ordinary causal prefill
   int32_t kv_splits;
   int64_t split_out_stride, split_lse_stride;
+  // A call with both kinds of request launches the prefill grid, then the
+  // decode grid right behind it on the same stream (programmatic dependent
+  // launch), the two sharing the SMs:
+  //   prefill grid, shared_sms > 0: it keeps about as many of the SMs as
+  //     its share of the estimated work (prefill tiles against decode
+  //     bytes, out of shared_sms), its other CTAs leave at once, so that
+  //     the decode grid -- launched when every prefill CTA has started or
+  //     left -- has the rest;
+  //   decode grid, after_prefill: its CTAs do not wait for the prefill grid;
+  //     one extra CTA (z = num_seqs) waits for it and exits, so that the
+  //     decode grid completes only after the prefill grid has.
+  //   no_decode: the host has shown that no request is short enough for the
+  //     decode kernel (no decode grid is launched); the prefill kernel flags
+  //     one that is as PKV_DEV_BAD_LENGTHS.
+  int32_t shared_sms;
+  int32_t after_prefill;
+  int32_t no_decode;
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
@@ -115,10 +132,11 @@ cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
 // `q_map`: q as [T][H][D] with a box of {64, G, 128/G}, 128-byte swizzle.
 // `kv_map`: the pool viewed as for the decode kernel but with a box of
 // {64, 16, 1, 1} (one 64-column chunk of 16 keys), 128-byte swizzle.
-// `priority` (0: the stream's own) is the launch's scheduling priority, a
-// value in the device's stream-priority range (lower runs first).
+// Launched with programmatic dependent launch: its CTAs start work after the
+// preceding grid has completed, and let the next grid launch as soon as
+// each has started.
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
-                           const CUtensorMap& kv_map, cudaStream_t stream, int priority = 0);
+                           const CUtensorMap& kv_map, cudaStream_t stream);
 
 // Cascade preparation: part_lse[0 .. n_lse) = -inf and tail_cu[i] = i for
 // i <= num_seqs.

@@ -157,7 +157,10 @@ struct Bars {
   int32_t abort;
   int32_t scan[kThreads / 32];
   uint32_t v_mask[kNS];  // boxes of the V stage that were loaded (bit b: keys 16b .. 16b+15)
+  float red[2][kThreads / 32];
 };
+
+static_assert(sizeof(Bars) <= 512, "the barriers fit below the work list");
 
 struct PrefillItem {
   int req, kvh, j0, j1, t0, qlen, L, kv_end, n_tiles;
@@ -198,7 +201,10 @@ __device__ __forceinline__ int prefill_units(const AttnParams& p, int r, int QP,
     if (qlen < 1 || L == 0) return 0;
     return ((qlen + QP - 1) / QP) * prefix_segment_count(L, p.kv_splits);
   }
-  if (qlen <= p.decode_max_q) return 0;  // short requests run on the decode kernel
+  if (qlen <= p.decode_max_q) {  // short requests run on the decode kernel
+    if (p.no_decode && qlen > 0 && flag) set_status(p.status, PKV_DEV_BAD_LENGTHS);
+    return 0;
+  }
   const int32_t L = __ldg(p.seq_lens + r);
   const bool bad_range =
       p.key_start ? (L < 1 || __ldg(p.key_start + r) < 0 || __ldg(p.query_start + r) < 0)
@@ -329,6 +335,62 @@ __device__ __forceinline__ WorkList prefill_work_list(const AttnParams& p, int* 
   wl.n = n;
   wl.sorted = true;
   return wl;
+}
+
+// Calibration of the SM split of a mixed call, measured on GB300: a
+// 128-key tile pair (two Q tiles) takes ~5800 cycles of an SM in this
+// kernel; the decode kernel streams ~40 bytes of K/V per cycle of an SM
+// when it has only some of the SMs.
+constexpr float kPairCycles = 5800.f;
+constexpr float kDecodeBytesPerCycle = 40.f;
+
+// The CTAs of this grid that take prefill work when a decode grid shares the
+// SMs: out of p.shared_sms, the prefill work's share of the estimated SM
+// time (its tile pairs against the decode requests' K/V bytes), at least 1.
+// All threads (two __syncthreads); every CTA computes the same value.
+__device__ __noinline__ int prefill_share(const AttnParams& p, int QP, float (*red)[kThreads / 32]) {
+  const int B = p.num_seqs;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int r0 = min(B, (int)threadIdx.x * per), r1 = min(B, r0 + per);
+  float pairs = 0.f, dkeys = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const int32_t t0 = __ldg(p.cu_seqlens + r), qlen = __ldg(p.cu_seqlens + r + 1) - t0;
+    const int32_t L = __ldg(p.seq_lens + r);
+    if (qlen < 1 || L < 1 || L > p.max_seq_len) continue;
+    if (qlen <= p.decode_max_q) {
+      dkeys += (float)L;
+      continue;
+    }
+    int64_t q0 = (int64_t)L - qlen;  // position of the first query among the keys
+    if (p.key_start) q0 = (int64_t)__ldg(p.query_start + r) - __ldg(p.key_start + r);
+    for (int j1 = min(qlen, QP);; j1 = min(qlen, j1 + QP)) {
+      const int64_t end = max((int64_t)0, min((int64_t)L, q0 + j1));
+      pairs += (float)max((int64_t)1, (end + kBN - 1) / kBN);
+      if (j1 == qlen) break;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pairs += __shfl_xor_sync(kFullMask, pairs, o);
+    dkeys += __shfl_xor_sync(kFullMask, dkeys, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = pairs;
+    red[1][warp] = dkeys;
+  }
+  __syncthreads();
+  float pt = 0.f, dt = 0.f;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    pt += red[0][w];
+    dt += red[1][w];
+  }
+  __syncthreads();
+  const float a = dt * (float)(p.num_kv_heads * p.head_dim * 4) / kDecodeBytesPerCycle;
+  const float b = pt * (float)p.num_kv_heads * kPairCycles;
+  const int S = p.shared_sms;
+  const int keep = a + b > 0.f ? S - (int)((float)S * a / (a + b) + 0.5f) : S;
+  return max(1, min(S, keep));
 }
 
 __device__ __forceinline__ PrefillItem prefill_item(const AttnParams& p, const WorkList& wl, int QP,
@@ -520,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int total_units = 0;
   const WorkList wl = prefill_work_list(p, list_base, bars->scan, QP, &total_units);  // syncs
   const int total = total_units * p.num_kv_heads;
-  if ((int)blockIdx.x >= total) {  // uniform; nothing allocated yet
+  const int active = p.shared_sms > 0 ? prefill_share(p, QP, bars->red) : (int)gridDim.x;  // syncs
+  if ((int)blockIdx.x >= min(total, active)) {  // uniform; nothing allocated yet
     if (threadIdx.x == 0) cta_finished(p);
     return;
   }
@@ -980,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
-                             const CUtensorMap& kv_map, cudaStream_t stream, int priority) {
+                             const CUtensorMap& kv_map, cudaStream_t stream) {
   using Lay = PrefillLayout<D>;
   const size_t smem = Lay::bytes(p.num_seqs);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -1002,22 +1065,20 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributePriority;
-  attr[1].val.priority = priority;
   cfg.attrs = attr;
-  cfg.numAttrs = priority != 0 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, q_map, kv_map, p);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
-                           const CUtensorMap& kv_map, cudaStream_t stream, int priority) {
-  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, kv_map, stream, priority);
-  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, kv_map, stream, priority);
+                           const CUtensorMap& kv_map, cudaStream_t stream) {
+  if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, kv_map, stream);
+  if (p.head_dim == 64) return launch_prefill_d<64>(p, q_map, kv_map, stream);
   return cudaErrorInvalidValue;
 }
 
