@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libpkv.so")
-SOURCES = ["kv_write.cu", "decode_mma.cu", "merge.cu", "prefill_tc.cu", "copy_blocks.cu", "cascade.cu",
+SOURCES = ["kv_write.cu", "decode_mma.cu", "merge.cu", "prefill_tc.cu", "copy_blocks.cu",
            "api.cpp",
            "api_noalloc.cu", "block_manager.cpp"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "launch.h"),

@@ -134,12 +134,11 @@ int32_t cascade_splits(int32_t num_groups, int32_t max_group_size, int32_t max_p
 }
 
 // Cascade workspace: partial outputs [S+1][B][H][D] fp32 and lse [S+1][B][H]
-// (S prefix segments, then the tail), the tail pass's cu_seqlens [B+1], then
-// the tail pass's own split-KV workspace (zero-filled once, like any
-// attention workspace).
+// (the tail, then S prefix segments), then the tail pass's own split-KV
+// workspace (zero-filled once, like any attention workspace).
 struct CascadeLayout {
   int32_t splits;
-  size_t lse_off, cu_off, ws_off, ws_bytes, ws_sched_off, total;
+  size_t lse_off, ws_off, ws_bytes, ws_sched_off, total;
 };
 
 CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_group_size,
@@ -149,8 +148,7 @@ CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_g
   c.splits = cascade_splits(num_groups, max_group_size, max_prefix_len, num_heads, num_kv_heads);
   const size_t rows = (size_t)(c.splits + 1) * num_seqs * num_heads;
   c.lse_off = round_up(rows * head_dim * sizeof(float), 256);
-  c.cu_off = c.lse_off + round_up(rows * sizeof(float), 256);
-  c.ws_off = c.cu_off + round_up((size_t)(num_seqs + 1) * sizeof(int32_t), 256);
+  c.ws_off = c.lse_off + round_up(rows * sizeof(float), 256);
   int32_t ps = 0, np = 1;
   resolve_partition(max_tail_len, -1, &ps, &np);
   const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, np);
@@ -530,73 +528,66 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
   char* ws = static_cast<char*>(workspace);
   float* part_out = reinterpret_cast<float*>(ws);
   float* part_lse = reinterpret_cast<float*>(ws + c.lse_off);
-  int32_t* tail_cu = reinterpret_cast<int32_t*>(ws + c.cu_off);
   const int64_t bh = (int64_t)num_seqs * num_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool prefixes = num_prefix_groups > 0 && max_prefix_len > 0;
 
   // Every check and tensor-map encoding happens before the first launch.
   // Tails: ordinary decode over each request's private blocks, one query per
-  // request (the cu_seqlens the preparation kernel writes).
+  // request (request i is query i: no cu_seqlens array; tail_lens stands in
+  // for it in the planning checks), into partial slot 0 -- or straight into
+  // `out` when there is no prefix.
   AttnPlan tails;
   pkv_status s = plan_attention(
-      &tails, part_out + (int64_t)c.splits * bh * head_dim, part_lse + (int64_t)c.splits * bh, q,
-      kv_pool, tail_tables, max_tail_blocks, tail_cu, tail_lens, num_seqs, num_seqs, 1,
-      max_tail_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, -1, nullptr,
-      nullptr, dev_status);
+      &tails, prefixes ? part_out : out, prefixes ? part_lse : out_lse, q, kv_pool, tail_tables,
+      max_tail_blocks, tail_lens, tail_lens, num_seqs, num_seqs, 1, max_tail_len, num_heads,
+      num_kv_heads, head_dim, block_size, num_blocks, scale, -1, nullptr, nullptr, dev_status);
   if (s != PKV_OK) return s;
+  tails.p.cu_seqlens = nullptr;
   if ((s = bind_workspace(&tails, ws + c.ws_off, c.ws_bytes)) != PKV_OK) return s;
   if ((s = encode_plan(&tails)) != PKV_OK) return s;
+  if (!prefixes) return launch_plan(tails, st);
   // Prefixes: every group's queries against its shared blocks, once, on the
-  // tensor cores (the prefill kernel in prefix mode), cut into key segments.
-  const bool prefixes = num_prefix_groups > 0 && max_prefix_len > 0;
+  // tensor cores (the prefill kernel in prefix mode), cut into key segments
+  // written to partial slots 1 .. S.
   AttnParams p = tails.p;
   CUtensorMap q_map{}, kv_box{};
-  if (prefixes) {
-    p.out = part_out;
-    p.out_lse = part_lse;
-    p.block_table = prefix_tables;
-    p.cu_seqlens = group_starts;
-    p.seq_lens = prefix_lens;
-    p.max_blocks = max_prefix_blocks;
-    p.num_seqs = num_prefix_groups;
-    p.num_tokens = num_seqs;
-    p.max_query_len = max_group_size;
-    p.max_seq_len = max_prefix_len;
-    p.part_size = 0;
-    p.num_parts = 1;
-    p.ws_out = nullptr;
-    p.ws_lse = nullptr;
-    p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
-    p.decode_max_q = 0;  // the prefix pass takes every group
-    p.decode_max_rows = 0;
-    p.prefix_mode = 1;
-    p.kv_splits = c.splits;
-    p.split_out_stride = bh * head_dim;
-    p.split_lse_stride = bh;
-    if (!encode_q_tiles(&q_map, q, num_seqs, num_heads, num_kv_heads, head_dim) ||
-        !encode_kv_view(&kv_box, kv_pool, num_blocks, block_size, num_kv_heads, head_dim, 1))
-      return PKV_ERR_CUDA;
-  }
-
-  // 1. empty prefix partials, one query per request for the tail pass
-  if (pkv::launch_cascade_prepare(part_lse, (int64_t)c.splits * bh, tail_cu, num_seqs, st) !=
-      cudaSuccess)
+  p.out = part_out + bh * head_dim;
+  p.out_lse = part_lse + bh;
+  p.block_table = prefix_tables;
+  p.cu_seqlens = group_starts;
+  p.seq_lens = prefix_lens;
+  p.max_blocks = max_prefix_blocks;
+  p.num_seqs = num_prefix_groups;
+  p.num_tokens = num_seqs;
+  p.max_query_len = max_group_size;
+  p.max_seq_len = max_prefix_len;
+  p.part_size = 0;
+  p.num_parts = 1;
+  p.ws_out = nullptr;
+  p.ws_lse = nullptr;
+  p.sched = reinterpret_cast<int32_t*>(ws + c.ws_off + c.ws_sched_off);
+  p.decode_max_q = 0;  // the prefix pass takes every group
+  p.decode_max_rows = 0;
+  p.prefix_mode = 1;
+  p.kv_splits = c.splits;
+  p.split_out_stride = bh * head_dim;
+  p.split_lse_stride = bh;
+  if (!encode_q_tiles(&q_map, q, num_seqs, num_heads, num_kv_heads, head_dim) ||
+      !encode_kv_view(&kv_box, kv_pool, num_blocks, block_size, num_kv_heads, head_dim, 1))
     return PKV_ERR_CUDA;
-  if (prefixes) {
-    // 2 + 3. the prefix pass (tensor cores; its grid sized for about a
-    // quarter of the SMs), then right behind it the tails (decode kernel)
-    // on the SMs it leaves; they write disjoint partial slots, and the tail
-    // grid completes only after the prefix pass has
-    if (pkv::launch_prefill(p, q_map, kv_box, st) != cudaSuccess) return PKV_ERR_CUDA;
-    AttnParams d = tails.p;
-    d.after_prefill = 1;
-    if (pkv::launch_decode_mma(d, tails.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
-  } else if ((s = launch_plan(tails, st)) != PKV_OK) {  // 2. tails only
-    return s;
-  }
-  // 4. merge every request's prefix segments and tail by log-sum-exp
-  return pkv::launch_lse_merge(out, out_lse, part_out, part_lse, c.splits + 1, bh, head_dim, st) ==
-                 cudaSuccess
+
+  // 1. the prefix pass (its grid sized for about a quarter of the SMs);
+  // 2. right behind it, on the SMs it leaves, the tails (their grid
+  // completes only after the prefix pass has); 3. every request's tail and
+  // prefix segments merged by log-sum-exp
+  if (pkv::launch_prefill(p, q_map, kv_box, st) != cudaSuccess) return PKV_ERR_CUDA;
+  AttnParams d = tails.p;
+  d.after_prefill = 1;
+  if (pkv::launch_decode_mma(d, tails.kv_rows, st) != cudaSuccess) return PKV_ERR_CUDA;
+  return pkv::launch_cascade_merge(out, out_lse, part_out, part_lse, bh, num_heads, head_dim,
+                                   group_starts, prefix_lens, num_prefix_groups, c.splits,
+                                   st) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

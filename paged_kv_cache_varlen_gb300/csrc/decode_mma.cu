@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // The request's lengths and the block ids of this warp's first chunks are
   // fetched together, one memory round trip before the first copy is issued
   // (the ids are read speculatively, bounded by the table row only).
-  const int32_t t0 = __ldg(p.cu_seqlens + i);
-  const int32_t t1 = __ldg(p.cu_seqlens + i + 1);
+  const int32_t t0 = p.cu_seqlens ? __ldg(p.cu_seqlens + i) : i;
+  const int32_t t1 = p.cu_seqlens ? __ldg(p.cu_seqlens + i + 1) : i + 1;
   const int32_t L = __ldg(p.seq_lens + i);
   const bool ranged = p.key_start != nullptr;
   const int32_t kstart = ranged ? __ldg(p.key_start + i) : 0;
@@ -476,8 +476,8 @@ __global__ void __launch_bounds__(128 * (WPR == 1 ? 1 : WPR / 4))
   // starts only once every attention CTA has passed its own wait on the
   // grids before it, so they are final; they are read (through L2) while the
   // attention grid is still running, off the path after its completion.
-  const int32_t t0 = __ldcg(p.cu_seqlens + i);
-  const int32_t t1 = __ldcg(p.cu_seqlens + i + 1);
+  const int32_t t0 = p.cu_seqlens ? __ldcg(p.cu_seqlens + i) : i;
+  const int32_t t1 = p.cu_seqlens ? __ldcg(p.cu_seqlens + i + 1) : i + 1;
   const int32_t L = __ldcg(p.seq_lens + i);
   griddep_wait();  // the attention grid and its partials are complete
   griddep_launch_dependents();

@@ -47,13 +47,26 @@ struct KvWriteParams {
 };
 
 // Attention problem shared by the decode, merge and prefill kernels.
+// Key segments of a shared prefix of L tokens in the cascade's prefix pass:
+// its 128-key tiles cut into segments of prefix_tiles_per_segment tiles, of
+// which prefix_segment_count are non-empty (at most `splits`).
+__host__ __device__ inline int prefix_tiles_per_segment(int L, int splits) {
+  const int t = (L + 127) / 128;
+  return (t + splits - 1) / splits;
+}
+__host__ __device__ inline int prefix_segment_count(int L, int splits) {
+  const int t = (L + 127) / 128;
+  const int tps = prefix_tiles_per_segment(L, splits);
+  return tps > 0 ? (t + tps - 1) / tps : 0;
+}
+
 struct AttnParams {
   float* out;                 // [T][H][D] fp32
   float* out_lse;             // [T][H] fp32 or null
   const uint16_t* q;          // [T][H][D] bf16
   const void* kv_pool;        // [2][NB][BS][Hkv][D] bf16
   const int32_t* block_table; // [B][max_blocks]
-  const int32_t* cu_seqlens;  // [B+1]
+  const int32_t* cu_seqlens;  // [B+1]; null: one query per request (request i is query i)
   const int32_t* seq_lens;    // [B]
   int32_t max_blocks;
   int32_t num_seqs, num_tokens, max_query_len, max_seq_len;
@@ -138,10 +151,17 @@ cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
                            const CUtensorMap& kv_map, cudaStream_t stream);
 
-// Cascade preparation: part_lse[0 .. n_lse) = -inf and tail_cu[i] = i for
-// i <= num_seqs.
-cudaError_t launch_cascade_prepare(float* part_lse, int64_t n_lse, int32_t* tail_cu,
-                                   int32_t num_seqs, cudaStream_t stream);
+// Shared-prefix (cascade) merge: row r of out (num_rows = B * H rows of
+// head_dim) from the tail partial (slot 0) and the prefix segments (slots
+// 1 .. segments of its request's group, prefix_segment_count of the group's
+// prefix length; none for a request outside every group), each slot
+// [num_rows][head_dim] fp32 with lse [num_rows]. Launched with programmatic
+// dependent launch (waits for the grid before it).
+cudaError_t launch_cascade_merge(float* out, float* out_lse, const float* part_out,
+                                 const float* part_lse, int64_t num_rows, int32_t num_heads,
+                                 int32_t head_dim, const int32_t* group_starts,
+                                 const int32_t* prefix_lens, int32_t num_groups, int32_t splits,
+                                 cudaStream_t stream);
 
 // Whole-block copies in the pool; block_vecs = 16-byte vectors in one
 // block of one half (K or V).

@@ -170,17 +170,7 @@ struct PrefillItem {
   int seg;  // key segment (prefix mode), else 0
 };
 
-// Prefix mode: the keys of a prefix of L tokens are cut into segments of
-// tiles_per_segment tiles; segment_count of them are non-empty.
-__device__ __forceinline__ int prefix_tiles_per_segment(int L, int splits) {
-  const int t = (L + kBN - 1) / kBN;
-  return (t + splits - 1) / splits;
-}
-__device__ __forceinline__ int prefix_segment_count(int L, int splits) {
-  const int t = (L + kBN - 1) / kBN;
-  const int tps = prefix_tiles_per_segment(L, splits);
-  return tps > 0 ? (t + tps - 1) / tps : 0;
-}
+static_assert(kBN == 128, "prefix segments count 128-key tiles");
 
 // Work units (pairs of query tiles) of request r (0 for requests of at most
 // decode_max_q queries, which the decode kernel takes);

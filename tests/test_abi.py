@@ -136,8 +136,8 @@ def test_cascade_workspace_size_arithmetic(lib):
     B, H, Hkv, D = 256, 32, 8, 128
 
     def expect(splits, tail_parts):
-        rows = (splits + 1) * B * H          # S prefix segments, then the tail
-        size = up(rows * D * 4) + up(rows * 4) + up((B + 1) * 4)
+        rows = (splits + 1) * B * H          # the tail, then S prefix segments
+        size = up(rows * D * 4) + up(rows * 4)
         if tail_parts > 1:                   # the tail pass's own split-KV partials
             trows = B * tail_parts * H
             size += up(trows * D * 4) + up(trows * 4)
@@ -188,7 +188,7 @@ def _cascade(lib, **over):
 
 
 @pytest.mark.parametrize("over,status", [
-    ({"head_dim": 96}, 2),            # rejected before the preparation kernel is launched
+    ({"head_dim": 96}, 2),            # rejected before the first launch
     ({"block_size": 8}, 2),
     ({"out": None}, 1),
     ({"workspace_bytes": 1024}, 4),

@@ -222,6 +222,27 @@ def test_device_errors_set_status_bits_and_spare_other_requests(oracle):
     assert dev.dev_status() & gu.pkv.DEV_BAD_SLOT
 
 
+def test_short_request_without_decode_grid_is_flagged(oracle):
+    """num_tokens = 200 rows of q with max_query_len 100 over two requests
+    shows that no request can be short, so no decode grid is launched;
+    cu_seqlens_q disagrees (request 1 has 4 queries): that request is flagged,
+    request 0 is still exact."""
+    w = wl.build("nodec", [300, 40], [100, 4], 32, 8, 128, seed=216)
+    ref_pool = oracle.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
+    ref_o, ref_l = oracle.paged_attention(w.q, ref_pool, w.block_table, w.cu_seqlens,
+                                          w.seq_lens, w.scale)
+    dev = gu.DeviceStep(w)
+    dev.write()
+    q = torch.zeros((200,) + tuple(dev.q.shape[1:]), dtype=dev.q.dtype, device="cuda")
+    q[:104] = dev.q
+    out = torch.full(tuple(q.shape), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full(tuple(q.shape[:2]), float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_attention_varlen(q, dev.pool, dev.table, dev.cu, dev.lens, 100, w.max_seq_len,
+                               out=out, out_lse=lse, scale=w.scale, dev_status=dev.status)
+    assert dev.dev_status() & gu.pkv.DEV_BAD_LENGTHS
+    gu.compare(out[:100], lse[:100], ref_o[:100], ref_l[:100])
+
+
 @pytest.mark.parametrize("P,T,H,D", [(1, 3, 4, 128), (5, 7, 32, 128), (64, 2, 8, 64),
                                      (3, 4, 2, 256), (2, 1, 1, 4)])
 def test_public_lse_merge(oracle, P, T, H, D):
