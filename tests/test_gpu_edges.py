@@ -222,6 +222,16 @@ def test_device_errors_set_status_bits_and_spare_other_requests(oracle):
     assert dev.dev_status() & gu.pkv.DEV_BAD_SLOT
 
 
+@pytest.mark.parametrize("partition_size", [16, 48, 128, 1024])
+def test_partition_sizes_with_verification_requests(oracle, partition_size):
+    """Split-KV partition sizes on a batch that mixes one-query requests
+    (split) with several-query verification requests (one partition each,
+    the causal limit per row)."""
+    w = wl.build("mqparts", [100, 257, 1030, 2049, 3001, 40, 777], [2, 8, 5, 3, 7, 4, 1],
+                 32, 8, 128, seed=217)
+    _run_and_check(oracle, w, partition_size)
+
+
 def test_short_request_without_decode_grid_is_flagged(oracle):
     """num_tokens = 200 rows of q with max_query_len 100 over two requests
     shows that no request can be short, so no decode grid is launched;
