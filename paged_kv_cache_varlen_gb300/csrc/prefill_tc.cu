@@ -12,47 +12,42 @@
 //   page 3 §3.4: FlashAttention -- S and P stay on chip, tile by tile, exact.
 //
 // GB300 design:
-//   * persistent CTAs, one per SM: every CTA builds the per-request prefix
-//     sum of work items in shared memory and takes items dynamically from a
-//     global ticket counter in the workspace (the busiest SM had 1.6x the
-//     mean work under a static round-robin); an item is (request, KV head,
-//     two consecutive query tiles A and B of 128/G queries each), later
-//     items (more keys) first. Tensor memory and barriers are set up once per CTA;
-//     requests short enough for the decode kernel (1 .. decode_max_q
-//     queries) give no items here;
+//   * persistent CTAs, one per SM: every CTA builds the list of work items in
+//     shared memory (heaviest request first) and takes items dynamically
+//     from a global ticket counter in the workspace; an item is (request, KV
+//     head, two consecutive query tiles A and B of 128/G queries each), later
+//     items (more keys) first. Tensor memory and barriers are set up once
+//     per CTA; requests short enough for the decode kernel (1 ..
+//     decode_max_q queries) give no items here. When a decode grid shares
+//     the call, the grid keeps about its share of the SMs (prefill tiles
+//     against decode bytes) and its other CTAs leave at once;
 //   * a Q tile is 128 rows = (128/G queries) x (G heads sharing the KV head),
 //     so one pass over the K/V pages serves the whole GQA group, and both Q
-//     tiles of the item share every K/V tile loaded: the gather from L2 (the
-//     bound of this kernel, ~12 B/cycle per SM) is paid once per two tiles;
-//   * Q arrives by TMA ({64, G, 128/G} boxes, 128-byte swizzle). K and V
-//     tiles of 128 keys are gathered page by page (block ids from
-//     block_table) by two producer warps with 16-byte cp.async copies
-//     written straight into the 128-byte-swizzled layout the MMA descriptors
-//     read (keys past the needed range are zero-filled), in separate 2-stage
-//     rings. (Paged 16-key TMA boxes were slower: ~200 cycles per 2 KB box
-//     per SM);
-//   * S = Q K^T (M=128, N=128, K=head_dim) and O += P V (M=128, N=head_dim,
-//     K=128) run as tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued
-//     by one thread. Tensor memory holds S_A, S_B, O_A, O_B (4 x 128
-//     columns); P is written back in place over the S columns it came from,
-//     as a bf16 high part and a bf16 remainder (P ~= hi + lo to ~2^-16
-//     relative; O accumulates hi*V + lo*V -- a single bf16 rounding of P puts
-//     few-key rows up to ~4e-3 off the exact result); P is the A operand
+//     tiles of the item share every K/V tile loaded;
+//   * Q, K and V arrive by TMA with the 128-byte swizzle the MMA descriptors
+//     read: Q in {64, G, 128/G} boxes, a 128-key K or V tile as 8 boxes of 16
+//     keys (one page run; block ids from block_table) per 64-column chunk,
+//     issued by one thread per role (warp 8: Q and K, warp 10: V) into
+//     2-stage rings. Warps 9, 11, 14 and 15 convert each V stage to fp16 in
+//     place, zeroing rows not loaded or past the needed keys;
+//   * S = Q K^T (M=128, N=64, K=head_dim, bf16) and O += P V (M=128,
+//     N=head_dim, K=16 per step, fp16) run as tcgen05.mma kind::f16 with
+//     fp32 accumulation in tensor memory: per Q tile two S buffers of 64
+//     columns and O (2 x (64 + 64 + 128) = 512 columns). P is written back
+//     as fp16 pairs over the S columns it came from and is the A operand
 //     straight from TMEM;
+//   * one issuing thread per Q tile (warps 12, 13): QK^T of the next S tile
+//     is issued right behind the PV of the current one, so S of tile j+1 is
+//     ready while the softmax works on tile j, and the softmax warps go from
+//     one tile to the next without waiting for the tensor core;
 //   * two softmax warpgroups, one per Q tile; thread r of a warpgroup owns
-//     TMEM lane (= Q row) r: pass 1 reads S in 32-column pieces for the row
-//     maximum, pass 2 re-reads them, applies the causal mask and the
-//     exp2-domain online softmax (lazy rescale when the maximum grows by more
-//     than 8) and stores P; O is rescaled in TMEM when needed. While one
-//     warpgroup computes its softmax, the tensor core works on the other
-//     tile's products (ping-pong);
-//   * warps 8-9 produce loads, warp 10 issues the MMAs in a fixed order that
-//     alternates the two Q tiles (PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)),
-//     so one tile's softmax overlaps the other tile's products;
-//   * the softmax of a tile every key of which is visible to the warp's rows
-//     skips the mask and uses packed fp32x2 arithmetic; P's bf16 high part
-//     and remainder are cut by bit operations (truncation: hi + lo is p to
-//     2^-14 relative) instead of conversions;
+//     TMEM lane (= Q row) r: it loads the row's 64 scores into registers
+//     (one TMEM round trip), takes the maximum, computes the probabilities
+//     with the exp2-domain online softmax (lazy rescale when the maximum
+//     grows by more than 8), stores them as fp16 pairs and adds the rounded
+//     values to the row sum (so that O and l see the same weights); O is
+//     rescaled in TMEM when needed; a tile every key of which is visible to
+//     the warp's rows skips the mask and uses packed fp32x2 arithmetic;
 //   * every wait is bounded; on a timeout the CTA drains its copies and
 //     MMAs, frees its TMEM and leaves with PKV_DEV_TIMEOUT set.
 #include <math.h>
