@@ -142,8 +142,18 @@ struct Bars {
   uint64_t v_full[kNS], v_empty[kNS];
   uint64_t v_landed[kNS];  // V copies arrived (bf16), not yet converted
   uint64_t s_full[kQT][kSB];  // QK^T of the S tile landed in buffer b of S_x
-  uint64_t p_ready[kQT];  // the warpgroup stored P_x (and rescaled O_x)
-  uint64_t o_done[kQT];   // PV of the tile finished (S_x free, O_x stable)
+  // the warpgroup stored P(g) of Q tile x (and rescaled O_x): barrier
+  // [x][g & 1], phase g >> 1. Two barriers, alternating by S tile: the
+  // softmax may run a tile ahead of the issuer (it waits for the previous PV
+  // only to rescale O), but not two (P(g + 2) needs QK(g + 2), issued after
+  // PV(g)), so a barrier is never two phases past its waiter.
+  uint64_t p_ready[kQT][2];
+  // PV(g) of Q tile x finished (O_x stable): barrier [x][g & 1], phase g >> 1.
+  // Two barriers, alternating by S tile: a waiter for PV(g) then always finds
+  // the barrier at PV(g)'s phase or the one after (PV(g - 2) is complete once
+  // S(g + 1) has been seen, PV(g + 2) cannot be issued before P(g + 2)), so
+  // the softmax needs to wait only when it rescales O.
+  uint64_t o_done[kQT][2];
   uint64_t o_free[kQT];   // the warpgroup's epilogue has read O_x
   uint64_t mma_done;
   uint64_t item_full[kRing], item_empty[kRing];
@@ -552,8 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < kQT; ++x) {
       for (int b = 0; b < kSB; ++b) mbar_init(smem_addr(&bars->s_full[x][b]), 1);
-      mbar_init(smem_addr(&bars->p_ready[x]), kBM / 32);  // one arrival per softmax warp
-      mbar_init(smem_addr(&bars->o_done[x]), 1);
+      for (int b = 0; b < 2; ++b)  // one arrival per softmax warp
+        mbar_init(smem_addr(&bars->p_ready[x][b]), kBM / 32);
+      for (int b = 0; b < 2; ++b) mbar_init(smem_addr(&bars->o_done[x][b]), 1);
       mbar_init(smem_addr(&bars->o_free[x]), kBM / 32);
     }
     mbar_init(smem_addr(&bars->mma_done), kQT);
@@ -774,7 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       static_assert(kNS == 2 && kSB == 2 && kBN == 2 * kSN, "two-way selects below");
       const uint32_t s_full_b[kSB] = {smem_addr(&bars->s_full[x][0]),
                                       smem_addr(&bars->s_full[x][1])};
-      const uint32_t o_done_b = smem_addr(&bars->o_done[x]);
+      const uint32_t o_done_b[2] = {smem_addr(&bars->o_done[x][0]),
+                                    smem_addr(&bars->o_done[x][1])};
       const uint32_t s_tmem = tmem + Lay::s_col(x, 0);
       const uint32_t o_tmem = tmem + Lay::o_col(x);
       constexpr uint32_t kHalf16 = (kSN * 128) >> 4;  // rows of half a K/V tile, in 16-byte units
@@ -804,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(o_tmem, p_tmem + Lay::p_col(kk), vd + (uint32_t)((kk * 16 * 128) >> 4), idesc_pv,
                   (!first || kk > 0) ? 1u : 0u);
         if (rel) umma_commit((kt & 1) ? v_empty_b[1] : v_empty_b[0]);
-        umma_commit(o_done_b);
+        umma_commit((g & 1) ? o_done_b[1] : o_done_b[0]);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return mbar_wait(smem_addr(bar), parity, p.status, abort);
@@ -826,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g = gs + j, kt = gt + (j >> 1), h = j & 1;
           // the first PV of an item overwrites O_x: the previous item's
           // epilogue must have read it
-          ok = wait(&bars->p_ready[x], g & 1) &&
+          ok = wait(&bars->p_ready[x][g & 1], (g >> 1) & 1) &&
                (h || wait(&bars->v_full[kt % kNS], (kt / kNS) & 1)) &&
                (j > 0 || gi == 0 || wait(&bars->o_free[x], (gi - 1) & 1));
           if (!ok) break;
@@ -950,14 +962,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         l = l * alpha + (rsa + rsb);
-        if (gg > 0) {
-          // the previous tile's PV has finished writing O_x (also keeps this
-          // warp within one phase of the o_done barrier)
-          ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), (gg - 1) & 1,
-                                               p.status, abort));
+        if (j > 0 && __any_sync(kFullMask, resc)) {
+          // O_x is rescaled once the previous tile's PV has finished writing it
+          ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x][(gg - 1) & 1]),
+                                               ((gg - 1) >> 1) & 1, p.status, abort));
           if (!ok) break;
           tc_fence_after();
-          if (j > 0 && __any_sync(kFullMask, resc)) {
+          {
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t v[32];
@@ -975,13 +986,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef PKV_TEST_HOLD_ARRIVAL
         if (g_pkv_test_hold_prefill && blockIdx.x == 0 && warp == 0 && gg == 0) continue;
 #endif
-        if (lane == 0) mbar_arrive(smem_addr(&bars->p_ready[x]));
+        if (lane == 0) mbar_arrive(smem_addr(&bars->p_ready[x][gg & 1]));
       }
       if (!ok) break;
       // ---- epilogue of the item: O / l -> out, lse
       const int last = gs + d.n_sub - 1;
-      ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x]), last & 1, p.status,
-                                           abort));
+      ok = __all_sync(kFullMask, mbar_wait(smem_addr(&bars->o_done[x][last & 1]),
+                                           (last >> 1) & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
