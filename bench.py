@@ -93,21 +93,24 @@ def split_parts(max_seq_len: int, partition_size: int) -> int:
 
 
 def attention_launches(w, partition_size: int, ci) -> int:
-    """Kernels one attention call launches: the decode grid, the split-KV
-    merge grid when requests split, the prefill grid when a request has more
-    queries than the decode kernel takes; the cascade call adds its prepare
-    kernel, the prefix pass and the final merge around the tail decode."""
+    """Kernels one attention call launches: the decode grid and, when
+    requests split, its merge grid; with requests longer than the decode
+    kernel takes, the prefill grid first, and the decode grids behind it only
+    when some request may be short (num_seqs * max_query_len - num_tokens >=
+    max_query_len - max(1, 32 / G)). The cascade call: the prefix pass, the
+    tail decode (and its merge grid when tails split) and the final merge;
+    the tail decode alone when there is no prefix."""
     if ci is not None:
         tail = 1 + (1 if split_parts(ci["max_tail_len"], -1) > 1 else 0)
-        return 1 + tail + (1 if len(ci["prefix_lens"]) else 0) + 1
+        prefixes = len(ci["prefix_lens"]) > 0 and ci["max_prefix_len"] > 0
+        return tail + (2 if prefixes else 0)
     group = w.num_heads // w.num_kv_heads
     dmq = max(1, 32 // group)
-    n = 1
-    if split_parts(w.max_seq_len, partition_size) > 1:
-        n += 1
-    if w.max_query_len > dmq:
-        n += 1
-    return n
+    decode = 1 + (1 if split_parts(w.max_seq_len, partition_size) > 1 else 0)
+    if w.max_query_len <= dmq:
+        return decode
+    may_be_short = w.num_seqs * w.max_query_len - w.num_tokens >= w.max_query_len - dmq
+    return 1 + (decode if may_be_short else 0)
 
 
 def pack_inputs(tensors: dict, align: int = 256):
