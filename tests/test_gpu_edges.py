@@ -95,6 +95,23 @@ def test_verification_steps_around_the_decode_cutoff(oracle, H, Hkv, D):
     _run_and_check(oracle, w)
 
 
+@pytest.mark.parametrize("case", ["decode_heavy", "prefill_heavy", "empty_requests"])
+def test_mixed_batches_at_the_ends_of_the_sm_split(oracle, case):
+    """With decodes in the call the prefill grid keeps about its share of the
+    SMs and its other CTAs leave at once: long decodes beside one small chunk
+    (the share clamps to a single prefill CTA), one long chunk beside a single
+    short decode, and requests of no query beside both kinds. The results do
+    not depend on the split."""
+    if case == "decode_heavy":
+        L, q = [8000, 7000, 6000, 5000, 4000, 3000, 2000, 1000] * 4 + [200], [1] * 32 + [40]
+    elif case == "prefill_heavy":
+        L, q = [2500, 300], [1000, 1]
+    else:
+        L, q = [300, 50, 1000, 700, 64], [0, 40, 1, 0, 3]
+    w = wl.build("split_" + case, L, q, 32, 8, 128, seed=219 + len(L))
+    _run_and_check(oracle, w)
+
+
 def test_full_prefill_without_prior_context(oracle):
     w = wl.build("fresh", [1, 2, 127, 128, 129, 600], [1, 2, 127, 128, 129, 600], 32, 8, 128,
                  seed=207)
