@@ -16,6 +16,8 @@ import threading
 
 import torch
 
+from . import debug_checks
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libpkv.so")
 
@@ -143,6 +145,8 @@ def kv_cache_write(kv_pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tens
         raise ValueError("k_new / v_new must be [num_tokens, num_kv_heads, head_dim]")
     if dev_status is not None:
         _need(dev_status, torch.int32, 1, "dev_status")
+    if debug_checks.enabled():
+        debug_checks.check_slot_mapping(slot_mapping, num_blocks=nb, block_size=bs)
     st = load_library().pkv_kv_cache_write(
         _ptr(kv_pool), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), t, nb, bs, hkv, d,
         _ptr(dev_status), _stream(stream, kv_pool.device))
@@ -190,6 +194,10 @@ def paged_attention_varlen(q: torch.Tensor, kv_pool: torch.Tensor, block_table: 
         _need(dev_status, torch.int32, 1, "dev_status")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if debug_checks.enabled():
+        debug_checks.check_attention_tables(
+            cu_seqlens, seq_lens, block_table, num_tokens=t, max_query_len=int(max_query_len),
+            max_seq_len=int(max_seq_len), num_blocks=nb, block_size=bs)
     need = attention_workspace_size(b, t, h, hkv, d, max_seq_len, partition_size)
     if need and workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
@@ -242,6 +250,11 @@ def paged_attention_varlen_range(q: torch.Tensor, kv_pool: torch.Tensor,
         _need(dev_status, torch.int32, 1, "dev_status")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if debug_checks.enabled():
+        debug_checks.check_attention_tables(
+            cu_seqlens, seq_lens, block_table, num_tokens=t, max_query_len=int(max_query_len),
+            max_seq_len=int(max_seq_len), num_blocks=nb, block_size=bs,
+            key_start=key_start_pos, query_start=query_start_pos)
     need = attention_workspace_size(b, t, h, hkv, d, max_seq_len, partition_size)
     if need and workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
@@ -310,6 +323,10 @@ def paged_attention_varlen_noalloc(q: torch.Tensor, kv_pool: torch.Tensor,
         _need(dev_status, torch.int32, 1, "dev_status")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if debug_checks.enabled():
+        debug_checks.check_attention_tables(
+            cu_seqlens, seq_lens, block_table, num_tokens=t, max_query_len=int(max_query_len),
+            max_seq_len=int(max_seq_len), num_blocks=nb, block_size=bs)
     st = load_library().pkv_paged_attention_varlen_noalloc(
         _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), _ptr(block_table),
         block_table.shape[1], _ptr(cu_seqlens), _ptr(seq_lens), b, t, int(max_query_len),

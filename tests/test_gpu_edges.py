@@ -270,6 +270,22 @@ def test_short_request_without_decode_grid_is_flagged(oracle):
     gu.compare(out[:100], lse[:100], ref_o[:100], ref_l[:100])
 
 
+def test_debug_checks_name_the_bad_entry(oracle, monkeypatch):
+    """With PKV_DEBUG_CHECKS=1 the binding checks the tables on the host
+    before each call: a bad block id raises, naming the entry, before any
+    launch; valid tables pass and the call runs as usual."""
+    w = wl.build("dbg", [40, 300, 50], [1, 1, 20], 32, 8, 128, seed=302)
+    dev = gu.DeviceStep(w)
+    monkeypatch.setenv("PKV_DEBUG_CHECKS", "1")
+    dev.write()
+    bad = w.block_table.copy()
+    bad[1, 3] = w.num_blocks + 5
+    with pytest.raises(ValueError, match=r"block_table\[1\]\[3\]"):
+        dev.attend(table=gu.i32_tensor(bad))
+    assert dev.dev_status() == 0   # nothing ran
+    _run_and_check(oracle, w)
+
+
 @pytest.mark.parametrize("P,T,H,D", [(1, 3, 4, 128), (5, 7, 32, 128), (64, 2, 8, 64),
                                      (3, 4, 2, 256), (2, 1, 1, 4)])
 def test_public_lse_merge(oracle, P, T, H, D):
