@@ -27,8 +27,9 @@
 //   * Q, K and V arrive by TMA with the 128-byte swizzle the MMA descriptors
 //     read: Q in {64, G, 128/G} boxes, a 128-key K or V tile as 8 boxes of 16
 //     keys (one page run; block ids from block_table) per 64-column chunk,
-//     issued by one thread per role (warp 8: Q and K, warp 10: V) into
-//     2-stage rings. Warps 9, 11, 14 and 15 convert each V stage to fp16 in
+//     issued by one thread per role (warp 14: Q and K, warp 15: V) into
+//     2-stage rings. Warps 8-11, one on each SM sub-partition (a stage is
+//     ready when its slowest converter is), convert each V stage to fp16 in
 //     place, zeroing rows not loaded or past the needed keys;
 //   * S = Q K^T (M=128, N=64, K=head_dim, bf16) and O += P V (M=128,
 //     N=head_dim, K=16 per step, fp16) run as tcgen05.mma kind::f16 with
@@ -75,12 +76,13 @@ constexpr int kSB = 2;                               // S buffers per Q tile
 constexpr int kNS = 2;                               // stages of each of the K and V rings
 constexpr int kSub = 16;                             // keys per TMA box
 constexpr int kSoftmaxThreads = kQT * kBM;           // warps 0 .. 7 (warpgroups 0, 1)
-constexpr int kProdWarp0 = kSoftmaxThreads / 32;     // warp 8: Q and K tiles
-constexpr int kVWarp0 = kProdWarp0 + 2;              // warp 10: V tiles
-constexpr int kMmaWarp = kVWarp0 + 2;                // warps 12, 13: MMA issue for Q tiles A, B
-constexpr int kConverters = 4 * 32;                  // warps 9, 11, 14, 15: V to fp16
+constexpr int kConvWarp0 = kSoftmaxThreads / 32;     // warps 8-11: V to fp16 (one per sub-partition)
+constexpr int kMmaWarp = kConvWarp0 + 4;             // warps 12, 13: MMA issue for Q tiles A, B
+constexpr int kProdWarp0 = kMmaWarp + 2;             // warp 14: Q and K tiles
+constexpr int kVWarp0 = kProdWarp0 + 1;              // warp 15: V tiles
+constexpr int kConverters = 4 * 32;
 __device__ __forceinline__ int converter_slot(int warp) {
-  return warp == kProdWarp0 + 1 ? 0 : warp == kVWarp0 + 1 ? 1 : warp - kMmaWarp;
+  return warp - kConvWarp0;
 }
 constexpr int kThreads = 512;                        // four warpgroups
 // registers per thread: launched with 128; the softmax warpgroups take 152,
@@ -599,11 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Each role changes its register budget at the top of its own branch (no
   // control-flow merge between the change and the code that relies on it):
-  // warpgroup 2 (producers) and 3 (MMA + idle warps) give registers back,
-  // warpgroups 0 and 1 (softmax) take them.
-  if (warp >= kProdWarp0) {
+  // warpgroups 2 (converters) and 3 (MMA issue, copies) give registers
+  // back, warpgroups 0 and 1 (softmax) take them.
+  if (warp >= kConvWarp0) {
     setmaxnreg_dec<kOtherRegs>();
-    // ===== producers: Q and the K tiles (warp 8), the V tiles (warp 10),
+    // ===== producers: Q and the K tiles (warp 14), the V tiles (warp 15),
     // all by TMA =====
     // A 128-key tile is 8 boxes of 16 keys (a 16-key run never crosses a
     // page: block_size is a multiple of 16), each box one TMA copy per
@@ -710,8 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(smem_addr(&bars->q_full), (q_issued - 1) & 1, nullptr);
       }
     } else if (warp != kMmaWarp && warp != kMmaWarp + 1) {
-      // ===== converters (warps 9, 11, 14, 15): each landed V stage to fp16
-      // in place =====
+      // ===== converters (warps 8-11, one per SM sub-partition): each landed
+      // V stage to fp16 in place =====
       // piece i of a stage (row i / RP, 16-byte column unit i % RP) is
       // converted by converter thread i mod 128 (rows not loaded, or past
       // the needed keys, are zeroed); the stage is then published to the
