@@ -99,7 +99,10 @@ __device__ __forceinline__ uint32_t swz(int token, int unit) {
   return (uint32_t)(line * 128 + (((unit & 7) ^ (line & 7)) << 4));
 }
 
-template <int D, int SPW, int MINB>
+// UNITQ: one query per request, request i being query i (no cu_seqlens
+// array is read; a separate instantiation, so that the prologue's loads stay
+// branch-free in both).
+template <int D, int SPW, int MINB, bool UNITQ>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
   constexpr int KS = D / 16;            // k-steps of QK^T
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // The request's lengths and the block ids of this warp's first chunks are
   // fetched together, one memory round trip before the first copy is issued
   // (the ids are read speculatively, bounded by the table row only).
-  const int32_t t0 = p.cu_seqlens ? __ldg(p.cu_seqlens + i) : i;
-  const int32_t t1 = p.cu_seqlens ? __ldg(p.cu_seqlens + i + 1) : i + 1;
+  const int32_t t0 = UNITQ ? i : __ldg(p.cu_seqlens + i);
+  const int32_t t1 = UNITQ ? i + 1 : __ldg(p.cu_seqlens + i + 1);
   const int32_t L = __ldg(p.seq_lens + i);
   const bool ranged = p.key_start != nullptr;
   const int32_t kstart = ranged ? __ldg(p.key_start + i) : 0;
@@ -575,8 +578,10 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   constexpr int SPW = PKV_DECODE_MMA_SPW, MINB = PKV_DECODE_MMA_MINB;
   constexpr size_t SLOT = 2 * kChunk * D * 2;
   const size_t smem = 1024 + kWarps * SPW * SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
-  auto kernel = decode_mma_kernel<D, SPW, MINB>;
-  static SmemLimit limit;
+  const bool unitq = p.cu_seqlens == nullptr;
+  auto kernel = unitq ? decode_mma_kernel<D, SPW, MINB, true> : decode_mma_kernel<D, SPW, MINB, false>;
+  static SmemLimit limit_cu, limit_unit;
+  SmemLimit& limit = unitq ? limit_unit : limit_cu;
   if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), (int)smem);
       e != cudaSuccess)
     return e;
