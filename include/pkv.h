@@ -297,7 +297,7 @@ pkv_status pkv_paged_attention_varlen_noalloc(
  * A request's context is its group's prefix followed by its tail. The prefix
  * pass runs every group's queries (members x heads as the rows of tensor-core
  * tiles) against the prefix blocks once, split into key segments, on about a
- * quarter of the SMs; the tails run through the decode kernel at the same
+ * fifth of the SMs; the tails run through the decode kernel at the same
  * time on the others (launched right behind the prefix pass on `stream`);
  * the partial results merge by log-sum-exp.
  * Errors: as pkv_paged_attention_varlen; PKV_DEV_BAD_LENGTHS for inconsistent

@@ -117,10 +117,12 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t he
 }
 
 // Shared-prefix (cascade) decode: key segments per prefix so that the
-// prefix pass spreads over about a quarter of a GPU's SMs (38 CTAs of its
+// prefix pass spreads over about a fifth of a GPU's SMs (30 CTAs of its
 // one-per-SM grid; the results do not depend on it): it runs beside the
-// tail decode, which keeps the other SMs busy from the start.
-constexpr int64_t kCascadeRefSMs = 38;
+// tail decode, which keeps the other SMs busy from the start. (Measured on
+// 4 groups of 64 members sharing 2048-token prefixes: 113.8 us per call
+// with one segment per group against 118.6 us with two.)
+constexpr int64_t kCascadeRefSMs = 30;
 
 int32_t cascade_splits(int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len,
                        int32_t num_heads, int32_t num_kv_heads) {
@@ -577,7 +579,7 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
       !encode_kv_view(&kv_box, kv_pool, num_blocks, block_size, num_kv_heads, head_dim, 1))
     return PKV_ERR_CUDA;
 
-  // 1. the prefix pass (its grid sized for about a quarter of the SMs);
+  // 1. the prefix pass (its grid sized for about a fifth of the SMs);
   // 2. right behind it, on the SMs it leaves, the tails (their grid
   // completes only after the prefix pass has); 3. every request's tail and
   // prefix segments merged by log-sum-exp

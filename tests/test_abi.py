@@ -143,13 +143,13 @@ def test_cascade_workspace_size_arithmetic(lib):
             size += up(trows * D * 4) + up(trows * 4)
         return size + 256                    # prefill work tickets
     # 4 groups of 64 members, 2048-token prefixes: 64 queries per work item at
-    # G = 4, so 4 x 1 x 8 = 32 items; ceil(38 / 32) = 2 key segments (the
-    # prefix pass takes about a quarter of the SMs, beside the tails)
-    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 1024, H, Hkv, D) == expect(2, 1)
+    # G = 4, so 4 x 1 x 8 = 32 items; ceil(30 / 32) = 1 key segment (the
+    # prefix pass takes about a fifth of the SMs, beside the tails)
+    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 1024, H, Hkv, D) == expect(1, 1)
     # tails up to 3000 tokens split into 3 partitions of 1024
-    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 3000, H, Hkv, D) == expect(2, 3)
-    # one small group: ceil(38 / 8) = 5 segments of the 16 tiles
-    assert lib.pkv_cascade_workspace_size(B, 1, 64, 2048, 1024, H, Hkv, D) == expect(5, 1)
+    assert lib.pkv_cascade_workspace_size(B, 4, 64, 2048, 3000, H, Hkv, D) == expect(1, 3)
+    # one small group: ceil(30 / 8) = 4 segments of the 16 tiles
+    assert lib.pkv_cascade_workspace_size(B, 1, 64, 2048, 1024, H, Hkv, D) == expect(4, 1)
     # no groups: one (empty) prefix slot and the tail
     assert lib.pkv_cascade_workspace_size(B, 0, 1, 0, 1024, H, Hkv, D) == expect(1, 1)
     # segments never outnumber the prefix's 128-key tiles (256 tokens: 2 tiles)
