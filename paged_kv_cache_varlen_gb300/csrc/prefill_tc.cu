@@ -335,10 +335,12 @@ __device__ __forceinline__ WorkList prefill_work_list(const AttnParams& p, int* 
 }
 
 // Calibration of the SM split of a mixed call, measured on GB300: a
-// 128-key tile pair (two Q tiles) takes ~5800 cycles of an SM in this
+// 128-key tile pair (two Q tiles) takes ~4800 cycles of an SM in this
 // kernel; the decode kernel streams ~40 bytes of K/V per cycle of an SM
-// when it has only some of the SMs.
-constexpr float kPairCycles = 5800.f;
+// when it has only some of the SMs. (Swept on a mixed step of 48 decodes
+// and four 512-query chunks: 3000, 3800, 4800, 5800 and 6300 cycles gave
+// 312, 285, 269, 271 and 272 us per call.)
+constexpr float kPairCycles = 4800.f;
 constexpr float kDecodeBytesPerCycle = 40.f;
 
 // The CTAs of this grid that take prefill work when a decode grid shares the
