@@ -473,6 +473,14 @@ __device__ __forceinline__ int read_item(Bars* bars, const AttnParams& p, int k,
   return it;
 }
 
+// 32 bytes to global memory in one store (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float* p, float a, float b, float c, float d, float e,
+                                             float f, float g, float h) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d), "f"(e), "f"(f), "f"(g), "f"(h)
+               : "memory");
+}
+
 // Two fp32 values as fp16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
@@ -874,6 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sa0 = tmem + lane_base + Lay::s_col(x, 0);
     const uint32_t oa = tmem + lane_base + Lay::o_col(x);
     const float sl2 = p.scale_log2;
+    const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
     bool ok = true;
     int gs = 0;  // S tiles of this Q tile so far (all items)
     for (int k = 0; ok; ++k) {
@@ -1002,17 +1011,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float* orow = p.out + d.seg * p.split_out_stride +
                     ((int64_t)(d.t0 + qj) * p.num_heads + d.kvh * G + g) * D;
+      // each thread writes its own row: 32-byte stores (whole sectors) when
+      // `out` allows them (row offsets are multiples of 32 bytes), else 16-byte
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
         PKV_TMEM_LD32(oa + 32 * c, u);
         tmem_wait_ld();
         if (row_valid) {
+          if (out32) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(orow + 32 * c + e) =
-                make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
-                            __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
+            for (int e = 0; e < 32; e += 8)
+              st_global_v8(orow + 32 * c + e, __uint_as_float(u[e]) * inv,
+                           __uint_as_float(u[e + 1]) * inv, __uint_as_float(u[e + 2]) * inv,
+                           __uint_as_float(u[e + 3]) * inv, __uint_as_float(u[e + 4]) * inv,
+                           __uint_as_float(u[e + 5]) * inv, __uint_as_float(u[e + 6]) * inv,
+                           __uint_as_float(u[e + 7]) * inv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(orow + 32 * c + e) =
+                  make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
+                              __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
+          }
         }
       }
       if (row_valid && p.out_lse)
