@@ -108,7 +108,9 @@ def attention_launches(w, partition_size: int, ci) -> int:
     dmq = max(1, 32 // group)
     decode = 1 + (1 if split_parts(w.max_seq_len, partition_size) > 1 else 0)
     if w.max_query_len <= dmq:
-        return decode
+        # several-query batches of at most 256 requests: the order kernel first
+        ordered = w.num_tokens > w.num_seqs and w.num_seqs <= 256
+        return decode + (1 if ordered else 0)
     may_be_short = w.num_seqs * w.max_query_len - w.num_tokens >= w.max_query_len - dmq
     return 1 + (decode if may_be_short else 0)
 

@@ -95,8 +95,10 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
  * pkv_attention_workspace_size -- bytes of scratch that
  * pkv_paged_attention_varlen needs for these sizes and this partition_size
  * (at least 256: the prefill kernel's work tickets; split-KV partials on top:
- * [num_seqs][P][H][D] + [num_seqs][P][H] fp32 for P partitions; 0 only for
- * invalid sizes). The caller allocates it (a 256-byte aligned
+ * [num_seqs][P][H][D] + [num_seqs][P][H] fp32 for P partitions; when
+ * num_tokens > num_seqs and num_seqs <= 256, [num_seqs] int32 more: the order
+ * in which a batch of several-query (verification) requests runs, longest
+ * context first; 0 only for invalid sizes). The caller allocates it (a 256-byte aligned
  * device buffer at least this large) and ZERO-FILLS it once before its first
  * use (it holds the counter from which prefill CTAs take their work items;
  * the split-KV partials need no clearing). Every call that

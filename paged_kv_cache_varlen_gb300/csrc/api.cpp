@@ -100,19 +100,32 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // which are zero between calls.
 constexpr size_t kSchedBytes = 256;
 
+// Batches of several-query (verification) requests run the decode grid in
+// longest-request-first order when they have at most this many requests:
+// their CTAs each stream a whole context, and in request order the longest
+// ones could start last.
+constexpr int32_t kOrderMaxSeqs = 256;
+
+bool decode_ordered(int32_t num_seqs, int32_t num_tokens) {
+  return num_tokens > num_seqs && num_seqs <= kOrderMaxSeqs;
+}
+
 struct WorkspaceLayout {
-  size_t lse_off, sched_off, total;
+  size_t lse_off, sched_off, order_off, total;
 };
 
+// [split-KV partials][lse][tickets][decode order: num_seqs int32, only for
+// batches decode_ordered() picks]
 WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                 int32_t nparts) {
-  WorkspaceLayout w{0, 0, 0};
+                                 int32_t nparts, bool ordered = false) {
+  WorkspaceLayout w{0, 0, 0, 0};
   if (nparts > 1) {
     const size_t rows = (size_t)num_seqs * nparts * num_heads;
     w.lse_off = round_up(rows * head_dim * sizeof(float), 256);
     w.sched_off = w.lse_off + round_up(rows * sizeof(float), 256);
   }
-  w.total = w.sched_off + kSchedBytes;
+  w.order_off = w.sched_off + kSchedBytes;
+  w.total = w.order_off + (ordered ? round_up((size_t)num_seqs * sizeof(int32_t), 256) : 0);
   return w;
 }
 
@@ -166,6 +179,7 @@ CascadeLayout cascade_layout(int32_t num_seqs, int32_t num_groups, int32_t max_g
 // tokens (a no-op).
 struct AttnPlan {
   AttnParams p{};
+  bool ordered = false;   // decode-only batch run in longest-request-first order
   CUtensorMap kv_rows{};  // decode: 16-key boxes of whole rows of one KV head
   CUtensorMap q_map{};    // prefill: {64, G, 128/G} boxes of q
   CUtensorMap kv_box{};   // prefill: 16-key boxes of one 64-column chunk
@@ -210,7 +224,9 @@ pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q
 
   int32_t ps = 0, np = 1;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
-  a->wl = workspace_layout(num_seqs, num_heads, head_dim, np);
+  a->ordered = max_query_len <= (32 / group > 1 ? 32 / group : 1) &&
+               decode_ordered(num_seqs, num_tokens);
+  a->wl = workspace_layout(num_seqs, num_heads, head_dim, np, a->ordered);
 
   AttnParams& p = a->p;
   p.out = out;
@@ -299,6 +315,7 @@ pkv_status bind_workspace(AttnPlan* a, void* workspace, size_t workspace_bytes) 
     return PKV_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   a->p.sched = reinterpret_cast<int32_t*>(ws + a->wl.sched_off);
+  if (a->ordered) a->p.order = reinterpret_cast<int32_t*>(ws + a->wl.order_off);
   if (a->p.num_parts > 1) {
     a->p.ws_out = reinterpret_cast<float*>(ws);
     a->p.ws_lse = reinterpret_cast<float*>(ws + a->wl.lse_off);
@@ -418,12 +435,13 @@ pkv_status pkv_kv_cache_write(void* kv_pool, const void* k_new, const void* v_ne
 size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len,
                                     int32_t partition_size) {
-  (void)num_tokens;
   (void)num_kv_heads;
   int32_t ps = 0, np = 1;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return 0;
-  return workspace_layout(num_seqs, num_heads, head_dim, np).total;
+  return workspace_layout(num_seqs, num_heads, head_dim, np,
+                          decode_ordered(num_seqs, num_tokens))
+      .total;
 }
 
 pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,

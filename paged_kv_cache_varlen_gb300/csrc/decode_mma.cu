@@ -100,9 +100,10 @@ __device__ __forceinline__ uint32_t swz(int token, int unit) {
 }
 
 // UNITQ: one query per request, request i being query i (no cu_seqlens
-// array is read; a separate instantiation, so that the prologue's loads stay
-// branch-free in both).
-template <int D, int SPW, int MINB, bool UNITQ>
+// array is read). ORDERED: grid slice z takes request p.order[z]. Separate
+// instantiations, so that every prologue's loads stay branch-free (a
+// run-time choice there cost up to 5 %).
+template <int D, int SPW, int MINB, bool UNITQ, bool ORDERED>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
   constexpr int KS = D / 16;            // k-steps of QK^T
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int kvh = blockIdx.x / nsub;
   const int sub = blockIdx.x - kvh * nsub;
   const int part = blockIdx.y;
-  const int i = blockIdx.z;
+  const int i = ORDERED ? __ldg(p.order + blockIdx.z) : (int)blockIdx.z;
   const bool leader = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
   // The request's lengths and the block ids of this warp's first chunks are
@@ -572,6 +573,27 @@ __global__ void __launch_bounds__(128 * (WPR == 1 ? 1 : WPR / 4))
 #define PKV_DECODE_MMA_SPW 2
 #endif
 
+// Longest context first: order[rank] = request, rank by descending seq_len
+// (ties by index); one CTA, at most 256 requests. Waits for the grid before
+// it (the KV write), so that the decode grid's wait on it covers that too.
+__global__ void __launch_bounds__(256) decode_order_kernel(const AttnParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int32_t lens[256];
+  const int B = p.num_seqs, t = threadIdx.x;
+  if (t < B) lens[t] = __ldg(p.seq_lens + t);
+  __syncthreads();
+  if (t < B) {
+    const int32_t l = lens[t];
+    int rank = 0;
+    for (int j = 0; j < B; ++j) {
+      const int32_t lj = lens[j];
+      rank += (lj > l || (lj == l && j < t)) ? 1 : 0;
+    }
+    p.order[rank] = t;
+  }
+}
+
 template <int D>
 cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
                                 cudaStream_t stream) {
@@ -579,9 +601,12 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   constexpr size_t SLOT = 2 * kChunk * D * 2;
   const size_t smem = 1024 + kWarps * SPW * SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
   const bool unitq = p.cu_seqlens == nullptr;
-  auto kernel = unitq ? decode_mma_kernel<D, SPW, MINB, true> : decode_mma_kernel<D, SPW, MINB, false>;
-  static SmemLimit limit_cu, limit_unit;
-  SmemLimit& limit = unitq ? limit_unit : limit_cu;
+  const bool ordered = p.order != nullptr && !unitq && !p.after_prefill && p.num_seqs <= 256;
+  auto kernel = unitq     ? decode_mma_kernel<D, SPW, MINB, true, false>
+                : ordered ? decode_mma_kernel<D, SPW, MINB, false, true>
+                          : decode_mma_kernel<D, SPW, MINB, false, false>;
+  static SmemLimit limit_cu, limit_unit, limit_ordered;
+  SmemLimit& limit = unitq ? limit_unit : ordered ? limit_ordered : limit_cu;
   if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), (int)smem);
       e != cudaSuccess)
     return e;
@@ -596,6 +621,14 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (ordered) {
+    cudaLaunchConfig_t ocfg = cfg;
+    ocfg.gridDim = dim3(1);
+    ocfg.blockDim = dim3(256);
+    ocfg.dynamicSmemBytes = 0;
+    if (cudaError_t e = cudaLaunchKernelEx(&ocfg, decode_order_kernel, p); e != cudaSuccess)
+      return e;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, kv_map, p);
   if (e != cudaSuccess || p.num_parts < 2) return e;
   // few partitions: a warp per row; many: eight warps split a row's

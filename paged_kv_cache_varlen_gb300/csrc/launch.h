@@ -114,6 +114,10 @@ struct AttnParams {
   int32_t shared_sms;
   int32_t after_prefill;
   int32_t no_decode;
+  // decode grid only: request of grid slice z is order[z] (null: z), written
+  // by a one-CTA kernel launched before the decode grid (longest context
+  // first)
+  int32_t* order;
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);

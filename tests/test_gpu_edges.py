@@ -112,6 +112,18 @@ def test_mixed_batches_at_the_ends_of_the_sm_split(oracle, case):
     _run_and_check(oracle, w)
 
 
+@pytest.mark.parametrize("n", [64, 300])
+def test_verification_batches_in_and_out_of_longest_first_order(oracle, n):
+    """Decode-only batches with several-query requests run longest context
+    first when they have at most 256 requests (and in request order beyond):
+    lengths with ties, both sides of the limit."""
+    rng = np.random.default_rng(230 + n)
+    q = rng.integers(1, 8, size=n, endpoint=True)
+    L = q + rng.choice([0, 17, 300, 300, 1024, 2000], size=n)
+    w = wl.build("order", L, q, 32, 8, 128, seed=231 + n)
+    _run_and_check(oracle, w)
+
+
 def test_full_prefill_without_prior_context(oracle):
     w = wl.build("fresh", [1, 2, 127, 128, 129, 600], [1, 2, 127, 128, 129, 600], 32, 8, 128,
                  seed=207)
