@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--extra", default=EXTRA_DEFAULT,
                     help="comma-separated workloads also timed device-resident in the same "
-                         "run and reported under 'workloads' ('none' to skip)")
+                         "run and reported under 'workloads' ('none' to skip); a name "
+                         "ending in '+cascade' runs it as the cascade call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target length of the oracle CPU-baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
@@ -392,7 +393,7 @@ def run_reference(args):
     return 0
 
 
-EXTRA_DEFAULT = "long_split_kv,spec_verify,mixed_step"
+EXTRA_DEFAULT = "long_split_kv,spec_verify,mixed_step,prefill_chunks,prefix_cow+cascade"
 
 
 class DeviceWorkload:
@@ -647,24 +648,30 @@ def run_ours(args):
     e2e_ms = e_start.elapsed_time(e_stop)
 
     # ---- the other workloads of the hot path, device-resident --------------
+    # (each at least 200 steps and 200 calls after at least 10 warm-up steps:
+    # they are cheap, and a few calls right after switching workloads would
+    # set their figures)
+    KE, WE = max(K, 200), max(W, 10)
     extras = {}
     extra_names = [] if args.extra in ("", "none") else args.extra.split(",")
     for name in extra_names:
-        if name == args.config:
+        cascade = name.endswith("+cascade")
+        base = name[:-len("+cascade")] if cascade else name
+        if base == args.config and cascade == args.cascade:
             continue
         del bufs, results
         torch.cuda.empty_cache()
-        we = rank_workload(name, rank)
-        RE = DeviceWorkload(we, dev, stream, -1, False, l2_bytes)
-        for k in range(W):
+        we = rank_workload(base, rank)
+        RE = DeviceWorkload(we, dev, stream, -1, cascade, l2_bytes)
+        for k in range(WE):
             RE.step(k=k)
         if dist is not None:
             dist.barrier()
-        e_total = RE.timed(lambda k: RE.step(k=k), K)
-        e_attn = RE.timed(lambda k: RE.attend(k=k), K)
+        e_total = RE.timed(lambda k: RE.step(k=k), KE)
+        e_attn = RE.timed(lambda k: RE.attend(k=k), KE)
         t = max_over_ranks({"total_ms": e_total, "attn_ms": e_attn}, dist, dev)
-        step_ms, attn_e_ms = t["total_ms"] / K, t["attn_ms"] / K
-        roof, pre = roofline_and_prefill(we, attn_e_ms)
+        step_ms, attn_e_ms = t["total_ms"] / KE, t["attn_ms"] / KE
+        roof, pre = roofline_and_prefill(we, attn_e_ms, RE.ci)
         extras[name] = {
             "num_seqs": we.num_seqs, "num_tokens": we.num_tokens,
             "kv_bytes_per_step": we.kv_bytes(), "step_us": step_ms * 1e3,
@@ -673,7 +680,8 @@ def run_ours(args):
             "query_tokens_per_s": world * we.num_tokens / (step_ms * 1e-3),
             "attention_us": attn_e_ms * 1e3, "roofline": roof, "prefill": pre,
             "l2": workload_config(we, -1, world, RE.n_pools, l2_bytes)["l2"],
-            "gpu_launches": RE.launches_per_step() * K + (RE.launches_per_step() - 1) * K}
+            "steps": KE, "warmup": WE,
+            "gpu_launches": RE.launches_per_step() * KE + (RE.launches_per_step() - 1) * KE}
         del RE, we
         bufs, results = None, None
         torch.cuda.empty_cache()
@@ -703,7 +711,7 @@ def run_ours(args):
                                "steps": n1}}
     if rank == 0:
         # the headline step (K) and attention calls (K), single calls (NP) and
-        # e2e steps (E), plus each extra workload's K steps and K calls
+        # e2e steps (E), plus each extra workload's KE steps and KE calls
         launches = R.launches_per_step()
         line = {
             "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
