@@ -492,6 +492,12 @@ class DeviceWorkload:
 
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
+        # Hold the stream (a bounded sleep of ~0.2 ms on the device, before
+        # the first event) while the host enqueues the first calls: the
+        # region then measures the device's time for the K calls, not the
+        # host's latency to issue the first one onto an idle GPU.
+        with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(400_000)
         a.record(self.stream)
         for k in range(K):
             fn(k)
