@@ -22,6 +22,7 @@ the max over ranks, ``value`` the total bytes of all ranks over that time.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -496,13 +497,21 @@ class DeviceWorkload:
         # the first event) while the host enqueues the first calls: the
         # region then measures the device's time for the K calls, not the
         # host's latency to issue the first one onto an idle GPU.
-        with torch.cuda.stream(self.stream):
-            torch.cuda._sleep(400_000)
-        a.record(self.stream)
-        for k in range(K):
-            fn(k)
-        b.record(self.stream)
-        torch.cuda.synchronize(self.dev)
+        # The host must stay ahead of the device for the whole region: the
+        # garbage collector is off inside it (a full collection can hold the
+        # host for tens of ms while the device drains its queue).
+        gc.collect()
+        gc.disable()
+        try:
+            with torch.cuda.stream(self.stream):
+                torch.cuda._sleep(400_000)
+            a.record(self.stream)
+            for k in range(K):
+                fn(k)
+            b.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+        finally:
+            gc.enable()
         return a.elapsed_time(b)
 
     def launches_per_step(self) -> int:
@@ -592,8 +601,11 @@ def run_ours(args):
         dist.barrier()
     total_ms = R.timed(lambda k: R.step(k=k), K)
     # the attention call alone, K calls back to back (the roofline's kernel
-    # time: its average launch duration over this region)
-    attn_avg_ms = R.timed(lambda k: R.attend(k=k), K) / K
+    # time: its average launch duration over this region), in three regions:
+    # the median region counts, so that one region disturbed on the host
+    # cannot set it; all three are reported
+    attn_regions_ms = [R.timed(lambda k: R.attend(k=k), K) / K for _ in range(3)]
+    attn_avg_ms = statistics.median(attn_regions_ms)
     if dist is not None:
         dist.barrier()
     # spread of single calls, each between its own pair of events (which
@@ -674,7 +686,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
         e_total = RE.timed(lambda k: RE.step(k=k), KE)
-        e_attn = RE.timed(lambda k: RE.attend(k=k), KE)
+        e_attn = statistics.median(RE.timed(lambda k: RE.attend(k=k), KE) for _ in range(3))
         t = max_over_ranks({"total_ms": e_total, "attn_ms": e_attn}, dist, dev)
         step_ms, attn_e_ms = t["total_ms"] / KE, t["attn_ms"] / KE
         roof, pre = roofline_and_prefill(we, attn_e_ms, RE.ci)
@@ -687,7 +699,7 @@ def run_ours(args):
             "attention_us": attn_e_ms * 1e3, "roofline": roof, "prefill": pre,
             "l2": workload_config(we, -1, world, RE.n_pools, l2_bytes)["l2"],
             "steps": KE, "warmup": WE,
-            "gpu_launches": RE.launches_per_step() * KE + (RE.launches_per_step() - 1) * KE}
+            "gpu_launches": RE.launches_per_step() * KE + (RE.launches_per_step() - 1) * 3 * KE}
         del RE, we
         bufs, results = None, None
         torch.cuda.empty_cache()
@@ -716,8 +728,8 @@ def run_ours(args):
                "single_core": {"value": sample.kv_bytes() / sec1 / 1e9, "unit": "GB/s",
                                "steps": n1}}
     if rank == 0:
-        # the headline step (K) and attention calls (K), single calls (NP) and
-        # e2e steps (E), plus each extra workload's KE steps and KE calls
+        # the headline step (K) and attention calls (3 x K), single calls (NP) and
+        # e2e steps (E), plus each extra workload's KE steps and 3 x KE calls
         launches = R.launches_per_step()
         line = {
             "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
@@ -729,6 +741,7 @@ def run_ours(args):
             # would repeat it 32 times
             "seqs_per_s_32_layers": world * w.num_seqs / (ms_per_step * 1e-3) / 32,
             "attention_us": {"back_to_back_mean": attn_avg_ms * 1e3,
+                             "back_to_back_regions": [x * 1e3 for x in attn_regions_ms],
                              "single_call_events": {
                                  "calls": len(attn_ms),
                                  "p10": 1e3 * float(np.percentile(attn_ms, 10)),
@@ -743,7 +756,7 @@ def run_ours(args):
                               "out per step; step k+1's inputs and step k-1's output move "
                               "while step k runs (two device buffer sets)"},
             "prefill": prefill_line,
-            "gpu_launches": (launches * K + (launches - 1) * (K + NP) + launches * E
+            "gpu_launches": (launches * K + (launches - 1) * (3 * K + NP) + launches * E
                              + sum(x["gpu_launches"] for x in extras.values())),
             "workloads": extras,
             "clocks": dict(clocks, soak_steps_before_timing=soak_steps),
