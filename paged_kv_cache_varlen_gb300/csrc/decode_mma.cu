@@ -410,6 +410,8 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // rows padded to D + 8 floats: the quads of 4 consecutive rows store to
   // disjoint banks; rows past the CTA's own are not stored at all
   constexpr int RS = D + 8;
+  static_assert((size_t)kWarps * kRows * (RS + 2) * sizeof(float) <= (size_t)kWarps * SPW * SLOT,
+                "the reduction buffers fit in the slots they reuse (one slot a warp does not)");
   float* red_o = reinterpret_cast<float*>(smem);       // [kWarps][kRows][RS]
   float* red_ml = red_o + kWarps * kRows * RS;         // [kWarps][kRows][2]
 #pragma unroll
