@@ -1,6 +1,7 @@
-// decode_mma.cu -- paged attention for query_len == 1 requests (decode),
-// with the two products of each 16-token chunk on the warp-level tensor-core
-// path (mma.sync m16n8k16: bf16 operands, fp32 accumulation).
+// decode_mma.cu -- paged attention for decode requests (query_len == 1) and
+// short verification steps (up to 32 (query, head) rows a request), with the
+// two products of each 16-token chunk on the warp-level tensor-core path
+// (mma.sync m16n8k16: bf16 operands, fp32 accumulation).
 //
 // Method (sources as cited in include/pkv.h):
 //   page 1 §04: GQA, kv_head = q_head / (num_heads / num_kv_heads); decode
@@ -21,8 +22,9 @@
 // to stream K/V.
 //
 // GB300 design (the pipeline is the one of the CUDA-core decode kernel):
-//   * one CTA = (request, KV head, subgroup of up to 16 query heads,
-//     partition); each K/V byte of a partition is read from HBM once;
+//   * one CTA = (request, KV head, subgroup of up to 16 (query, head) rows,
+//     partition); each K/V byte of a partition is read from HBM once by
+//     each subgroup (one subgroup for a decode);
 //   * 4 warps, each with SPW private slots; a slot holds one 16-token chunk
 //     of K and of V for this KV head, fetched by one TMA load each (box of
 //     16 rows x head_dim, laid out as the rows' first 128-byte halves then
@@ -33,7 +35,7 @@
 //     domain with lazy rescaling (the running maximum moves only when a score
 //     exceeds it by more than 8); P goes straight from the accumulator
 //     registers into A fragments as a bf16 high part and a bf16 remainder
-//     (p ~= hi + lo to ~2^-16, as the prefill kernel does), and O += P V
+//     (p ~= hi + lo to ~2^-16), and O += P V
 //     with V rows from ldmatrix.trans; V rows of tokens past the context are
 //     zeroed first (P is 0 there, and 0 * NaN is not);
 //   * end: warps merge through shared memory; a split request's partitions
@@ -42,7 +44,10 @@
 //     (per-CTA timelines showed the CTA that merged in-kernel spending ~8 us
 //     of dependent memory round trips at the end of the grid);
 //   * the prologue reads the request's lengths and the first block ids in
-//     one round trip, so the first copies leave ~1 round trip earlier.
+//     one round trip, so the first copies leave ~1 round trip earlier;
+//   * decode-only batches with several-query requests (at most 256) run
+//     longest context first: a one-CTA kernel before the grid ranks the
+//     lengths, and grid slice z takes the request of rank z.
 #include <math.h>
 
 #include "common.cuh"
