@@ -96,7 +96,9 @@ def split_parts(max_seq_len: int, partition_size: int) -> int:
 
 def attention_launches(w, partition_size: int, ci) -> int:
     """Kernels one attention call launches: the decode grid and, when
-    requests split, its merge grid; with requests longer than the decode
+    requests split, its merge grid; before them, for a decode-only batch with
+    several-query requests and at most 256 requests, the one-CTA kernel that
+    orders the requests longest first; with requests longer than the decode
     kernel takes, the prefill grid first, and the decode grids behind it only
     when some request may be short (num_seqs * max_query_len - num_tokens >=
     max_query_len - max(1, 32 / G)). The cascade call: the prefix pass, the

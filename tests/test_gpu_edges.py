@@ -112,7 +112,7 @@ def test_mixed_batches_at_the_ends_of_the_sm_split(oracle, case):
     _run_and_check(oracle, w)
 
 
-@pytest.mark.parametrize("n", [64, 300])
+@pytest.mark.parametrize("n", [64, 256, 300])
 def test_verification_batches_in_and_out_of_longest_first_order(oracle, n):
     """Decode-only batches with several-query requests run longest context
     first when they have at most 256 requests (and in request order beyond):
