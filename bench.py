@@ -495,21 +495,25 @@ class DeviceWorkload:
 
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
-        # Hold the stream (a bounded sleep of ~0.2 ms on the device, before
-        # the first event) while the host enqueues the first calls: the
-        # region then measures the device's time for the K calls, not the
-        # host's latency to issue the first one onto an idle GPU.
+        # Hold the stream (a bounded sleep on the device, before the first
+        # event) while the host enqueues the calls: ~150 us a call, at least
+        # 0.2 ms and at most 20 ms. The region then measures the device's
+        # time for the K calls, not the host's latency to issue them (a step
+        # of two API calls takes the host about as long as the device).
         # The host must stay ahead of the device for the whole region: the
         # garbage collector is off inside it (a full collection can hold the
         # host for tens of ms while the device drains its queue).
         gc.collect()
         gc.disable()
         try:
+            hold_us = min(20_000, max(200, 150 * K))
             with torch.cuda.stream(self.stream):
-                torch.cuda._sleep(400_000)
+                torch.cuda._sleep(2_000 * hold_us)  # cycles at ~2 GHz
             a.record(self.stream)
+            t0 = time.perf_counter()
             for k in range(K):
                 fn(k)
+            self.last_host_us = (time.perf_counter() - t0) * 1e6 / K
             b.record(self.stream)
             torch.cuda.synchronize(self.dev)
         finally:
@@ -602,11 +606,13 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     total_ms = R.timed(lambda k: R.step(k=k), K)
+    step_host_us = R.last_host_us
     # the attention call alone, K calls back to back (the roofline's kernel
     # time: its average launch duration over this region), in three regions:
     # the median region counts, so that one region disturbed on the host
     # cannot set it; all three are reported
     attn_regions_ms = [R.timed(lambda k: R.attend(k=k), K) / K for _ in range(3)]
+    attn_host_us = R.last_host_us
     attn_avg_ms = statistics.median(attn_regions_ms)
     if dist is not None:
         dist.barrier()
@@ -736,7 +742,8 @@ def run_ours(args):
         line = {
             "metric": "paged decode attention KV GB/s", "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms_per_step, "host_enqueue_us_per_step": step_host_us,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "seqs_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
             # one attention layer per step; a 32-layer model's decode step
@@ -744,6 +751,7 @@ def run_ours(args):
             "seqs_per_s_32_layers": world * w.num_seqs / (ms_per_step * 1e-3) / 32,
             "attention_us": {"back_to_back_mean": attn_avg_ms * 1e3,
                              "back_to_back_regions": [x * 1e3 for x in attn_regions_ms],
+                             "host_enqueue_us_per_call": attn_host_us,
                              "single_call_events": {
                                  "calls": len(attn_ms),
                                  "p10": 1e3 * float(np.percentile(attn_ms, 10)),
