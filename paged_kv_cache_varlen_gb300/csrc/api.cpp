@@ -221,6 +221,10 @@ pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   const int32_t group = num_heads / num_kv_heads;
   if (max_query_len > 1 && (group > 128 || (128 % group) != 0)) return PKV_ERR_UNSUPPORTED;
+  // requests longer than the decode kernel takes: the prefill kernel's work
+  // list of num_seqs requests must fit its shared memory
+  if (max_query_len > (32 / group > 1 ? 32 / group : 1) && !pkv::prefill_fits(num_seqs, head_dim))
+    return PKV_ERR_UNSUPPORTED;
 
   int32_t ps = 0, np = 1;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
@@ -536,7 +540,8 @@ pkv_status pkv_cascade_decode(float* out, float* out_lse, const void* q, const v
     return PKV_ERR_INVALID_ARG;
   if (max_tail_len < 1 || max_tail_blocks <= 0) return PKV_ERR_INVALID_ARG;
   const int32_t group = num_heads / num_kv_heads;
-  if (num_prefix_groups > 0 && max_prefix_len > 0 && (group > 128 || (128 % group) != 0))
+  if (num_prefix_groups > 0 && max_prefix_len > 0 &&
+      (group > 128 || (128 % group) != 0 || !pkv::prefill_fits(num_prefix_groups, head_dim)))
     return PKV_ERR_UNSUPPORTED;
   if ((int64_t)max_prefix_blocks * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   const CascadeLayout c = cascade_layout(num_seqs, num_prefix_groups, max_group_size,

@@ -155,6 +155,11 @@ cudaError_t launch_decode_mma(const AttnParams& p, const CUtensorMap& kv_map,
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
                            const CUtensorMap& kv_map, cudaStream_t stream);
 
+// Whether the prefill kernel's shared memory (its K/V/Q stages plus the work
+// list of num_seqs requests) fits the 227 KB a CTA may have: up to 8575
+// requests at head_dim 128, 33151 at 64. False for other head dims.
+bool prefill_fits(int32_t num_seqs, int32_t head_dim);
+
 // Shared-prefix (cascade) merge: row r of out (num_rows = B * H rows of
 // head_dim) from the tail partial (slot 0) and the prefix segments (slots
 // 1 .. segments of its request's group, prefix_segment_count of the group's

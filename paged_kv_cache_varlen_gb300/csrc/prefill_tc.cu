@@ -1096,6 +1096,13 @@ cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& q_map,
 
 }  // namespace
 
+bool prefill_fits(int32_t num_seqs, int32_t head_dim) {
+  if (num_seqs < 0) return false;
+  if (head_dim == 128) return PrefillLayout<128>::bytes(num_seqs) <= 227 * 1024;
+  if (head_dim == 64) return PrefillLayout<64>::bytes(num_seqs) <= 227 * 1024;
+  return false;
+}
+
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& q_map,
                            const CUtensorMap& kv_map, cudaStream_t stream) {
   if (p.head_dim == 128) return launch_prefill_d<128>(p, q_map, kv_map, stream);

@@ -97,6 +97,19 @@ def test_attention_rejects_before_launch(lib, over, status):
     assert _attn(lib, **over) == status
 
 
+@pytest.mark.parametrize("head_dim, limit", [(128, 8575), (64, 33151)])
+def test_prefill_request_limit(lib, head_dim, limit):
+    # a call with prefill work (max_query_len above 32 / G) keeps the prefill
+    # kernel's work list in shared memory: at the limit the call gets past
+    # that check (and stops at the missing workspace), one request more is
+    # unsupported; decode-only calls are not limited by it
+    big = dict(max_query_len=64, max_seq_len=64, head_dim=head_dim)
+    assert _attn(lib, num_seqs=limit, num_tokens=limit, **big) == 4
+    assert _attn(lib, num_seqs=limit + 1, num_tokens=limit + 1, **big) == 2
+    assert _attn(lib, num_seqs=limit + 1, num_tokens=limit + 1, head_dim=head_dim,
+                 max_seq_len=4096, partition_size=0) == 4
+
+
 def test_empty_batch_is_a_no_op(lib):
     assert _attn(lib, num_tokens=0, out=None, q=None) == 0
 
@@ -192,6 +205,7 @@ def _cascade(lib, **over):
     ({"block_size": 8}, 2),
     ({"out": None}, 1),
     ({"workspace_bytes": 1024}, 4),
+    ({"num_prefix_groups": 8576, "num_seqs": 8576}, 2),   # prefix pass work list too large
     ({}, 3),                          # every check passes: the first CUDA step fails here
 ])
 def test_cascade_rejects_before_any_launch(lib, over, status):
