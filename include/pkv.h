@@ -103,7 +103,9 @@ pkv_status pkv_kv_cache_write(void *kv_pool, const void *k_new, const void *v_ne
  * [num_seqs][P][H][D] + [num_seqs][P][H] fp32 for P partitions; when
  * num_tokens > num_seqs and num_seqs <= 256, [num_seqs] int32 more: the order
  * in which a batch of several-query (verification) requests runs, longest
- * context first; 0 only for invalid sizes). The caller allocates it (a 256-byte aligned
+ * context first; 0 only for invalid sizes and for more than 65535
+ * partitions a request, which pkv_paged_attention_varlen refuses as
+ * PKV_ERR_UNSUPPORTED). The caller allocates it (a 256-byte aligned
  * device buffer at least this large) and ZERO-FILLS it once before its first
  * use (it holds the counter from which prefill CTAs take their work items;
  * the split-KV partials need no clearing). Every call that

@@ -26,6 +26,8 @@ using pkv::AttnParams;
 // 32K-128K; fewer, longer partitions amortise each CTA's prologue/epilogue).
 constexpr int32_t kAutoPartition = 1024;
 constexpr int32_t kMaxAutoParts = 32;
+// partitions of one request at most (the decode grid's y dimension)
+constexpr int32_t kMaxParts = 65535;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -228,6 +230,7 @@ pkv_status plan_attention(AttnPlan* a, float* out, float* out_lse, const void* q
 
   int32_t ps = 0, np = 1;
   if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return PKV_ERR_INVALID_ARG;
+  if (np > kMaxParts) return PKV_ERR_UNSUPPORTED;  // the decode grid's y dimension
   a->ordered = max_query_len <= (32 / group > 1 ? 32 / group : 1) &&
                decode_ordered(num_seqs, num_tokens);
   a->wl = workspace_layout(num_seqs, num_heads, head_dim, np, a->ordered);
@@ -442,7 +445,7 @@ size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_
   (void)num_kv_heads;
   int32_t ps = 0, np = 1;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
-  if (!resolve_partition(max_seq_len, partition_size, &ps, &np)) return 0;
+  if (!resolve_partition(max_seq_len, partition_size, &ps, &np) || np > kMaxParts) return 0;
   return workspace_layout(num_seqs, num_heads, head_dim, np,
                           decode_ordered(num_seqs, num_tokens))
       .total;

@@ -110,6 +110,17 @@ def test_prefill_request_limit(lib, head_dim, limit):
                  max_seq_len=4096, partition_size=0) == 4
 
 
+def test_partition_count_limit(lib):
+    # 16-token partitions: 65535 of them per request is the most the decode
+    # grid takes (the call then stops at the missing workspace); one more is
+    # unsupported, and the workspace query gives 0 for it
+    at, over = 65535 * 16, 65535 * 16 + 1
+    assert _attn(lib, max_seq_len=at, max_blocks=at // 16, partition_size=16) == 4
+    assert _attn(lib, max_seq_len=over, max_blocks=at // 16 + 1, partition_size=16) == 2
+    assert lib.pkv_attention_workspace_size(1, 1, 4, 2, 128, at, 16) > 0
+    assert lib.pkv_attention_workspace_size(1, 1, 4, 2, 128, over, 16) == 0
+
+
 def test_empty_batch_is_a_no_op(lib):
     assert _attn(lib, num_tokens=0, out=None, q=None) == 0
 
