@@ -339,7 +339,8 @@ __device__ __forceinline__ WorkList prefill_work_list(const AttnParams& p, int* 
 // kernel; the decode kernel streams ~40 bytes of K/V per cycle of an SM
 // when it has only some of the SMs. (Swept on a mixed step of 48 decodes
 // and four 512-query chunks: 3000, 3800, 4800, 5800 and 6300 cycles gave
-// 312, 285, 269, 271 and 272 us per call.)
+// 312, 285, 269, 271 and 272 us per call; with the current kernel 4400, 4800,
+// 5100 and 5400 gave 273.5, 270.0, 270.0 and 271.2 us on one box.)
 constexpr float kPairCycles = 4800.f;
 constexpr float kDecodeBytesPerCycle = 40.f;
 
