@@ -124,6 +124,21 @@ def test_verification_batches_in_and_out_of_longest_first_order(oracle, n):
     _run_and_check(oracle, w)
 
 
+@pytest.mark.parametrize("H,Hkv", [(32, 8), (8, 8)])
+def test_verification_batches_head_dim_64(oracle, H, Hkv):
+    """The longest-first decode grid at head_dim 64: G = 4 (up to 8 queries,
+    32 rows a request) and G = 1 (up to 32 queries, two 16-row subgroups),
+    with one-query requests long enough to be split among them."""
+    G = H // Hkv
+    dmq = max(1, 32 // G)
+    rng = np.random.default_rng(240 + G)
+    n = 48
+    q = rng.integers(1, dmq, size=n, endpoint=True)
+    L = q + rng.choice([0, 5, 200, 700, 1500, 3000], size=n)
+    w = wl.build("verify64", L, q, H, Hkv, 64, seed=241 + G)
+    _run_and_check(oracle, w)
+
+
 def test_full_prefill_without_prior_context(oracle):
     w = wl.build("fresh", [1, 2, 127, 128, 129, 600], [1, 2, 127, 128, 129, 600], 32, 8, 128,
                  seed=207)

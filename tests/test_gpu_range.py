@@ -27,10 +27,10 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _batch():
+def _batch(head_dim=128):
     # decodes (one split into partitions), a verification step, two prefill
-    # chunks (one with no prior context), 32/8 heads, D 128
-    return wl.build("range", [6000, 700, 1800, 520, 2400], [1, 1, 300, 5, 512], 32, 8, 128,
+    # chunks (one with no prior context), 32/8 heads, D 128 (or 64)
+    return wl.build("range", [6000, 700, 1800, 520, 2400], [1, 1, 300, 5, 512], 32, 8, head_dim,
                     seed=41)
 
 
@@ -93,7 +93,16 @@ def _compare_pieces(out, lse, ref_o, ref_l):
 
 @pytest.mark.parametrize("case", ["head", "tail", "middle", "past_the_queries", "whole"])
 def test_range_piece_matches_oracle(oracle, case):
-    w = _batch()
+    _check_case(oracle, case, 128)
+
+
+@pytest.mark.parametrize("case", ["middle", "past_the_queries", "whole"])
+def test_range_piece_head_dim_64(oracle, case):
+    _check_case(oracle, case, 64)
+
+
+def _check_case(oracle, case, head_dim):
+    w = _batch(head_dim)
     ref_pool = oracle.kv_cache_write(w.pool, w.k_new, w.v_new, w.slot_mapping)
     dev = gu.DeviceStep(w)
     dev.write()
