@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--cascade", action="store_true",
                     help="prefix_cow only: read each shared prefix once per group "
                          "(pkv_cascade_decode) instead of once per request")
+    ap.add_argument("--separate-write", action="store_true",
+                    help="time each step as pkv_kv_cache_write then the attention call, "
+                         "instead of the combined pkv_paged_attention_varlen_append")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--extra", default=EXTRA_DEFAULT,
                     help="comma-separated workloads also timed device-resident in the same "
@@ -413,6 +416,7 @@ class DeviceWorkload:
 
         self.w, self.dev, self.stream, self.pkv = w, dev, stream, pkv
         self.partition_size = partition_size
+        self.separate_write = False
         T, H, D = w.q.shape
 
         def bf16(a):
@@ -482,10 +486,22 @@ class DeviceWorkload:
             ev[1].record(self.stream)
 
     def step(self, dd=None, res=None, k=0):
+        """One step: the KV write and the attention call. By default in one
+        call (pkv_paged_attention_varlen_append); the cascade call, and every
+        call with separate_write set, as the two calls one after the other."""
         dd = self.d if dd is None else dd
-        self.pkv.kv_cache_write(self.pools[k % self.n_pools], dd["k_new"], dd["v_new"],
-                                dd["slots"], stream=self.stream)
-        self.attend(dd, res=res, k=k)
+        pool = self.pools[k % self.n_pools]
+        if self.ci is not None or self.separate_write:
+            self.pkv.kv_cache_write(pool, dd["k_new"], dd["v_new"], dd["slots"],
+                                    stream=self.stream)
+            self.attend(dd, res=res, k=k)
+            return
+        w = self.w
+        o, ls = (self.out, self.lse) if res is None else res
+        self.pkv.paged_attention_varlen_append(
+            dd["q"], pool, dd["k_new"], dd["v_new"], dd["slots"], dd["table"], dd["cu"],
+            dd["lens"], w.max_query_len, w.max_seq_len, out=o, out_lse=ls, scale=w.scale,
+            partition_size=self.partition_size, workspace=self.ws, stream=self.stream)
 
     def timed(self, fn, K: int) -> float:
         """ms of K calls of fn(k) back to back between one pair of events (an
@@ -581,6 +597,7 @@ def run_ours(args):
     w = rank_workload(args.config, rank)
     T, H, D = w.q.shape
     R = DeviceWorkload(w, dev, stream, args.partition_size, args.cascade, l2_bytes)
+    R.separate_write = args.separate_write
     W = max(3, args.warmup)
     for k in range(W):
         R.step(k=k)
@@ -689,6 +706,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         we = rank_workload(base, rank)
         RE = DeviceWorkload(we, dev, stream, -1, cascade, l2_bytes)
+        RE.separate_write = args.separate_write
         for k in range(WE):
             RE.step(k=k)
         if dist is not None:
@@ -772,6 +790,10 @@ def run_ours(args):
             "clocks": dict(clocks, soak_steps_before_timing=soak_steps),
             "cpu_baseline": cpu,
         }
+        line["config"]["step"] = ("pkv_kv_cache_write + " + ("pkv_cascade_decode" if R.ci is not None
+                                                              else "pkv_paged_attention_varlen")
+                                  if R.ci is not None or R.separate_write
+                                  else "pkv_paged_attention_varlen_append (KV write + attention)")
         if R.ci is not None:
             line["config"]["attention"] = "cascade: each shared prefix read once per group"
         print(json.dumps(line), flush=True)

@@ -188,6 +188,42 @@ pkv_status pkv_paged_attention_varlen(float *out, float *out_lse, const void *q,
                                       void *stream);
 
 /*
+ * pkv_paged_attention_varlen_append -- one step's KV write and attention in
+ * one call: pkv_kv_cache_write(kv_pool, k_new, v_new, slot_mapping, ...)
+ * followed by pkv_paged_attention_varlen(...) over the same pool ([page 1]
+ * §02: a step appends its tokens' K/V to the cache through slot_mapping, then
+ * attends over it). Arguments: those of the two calls (k_new, v_new
+ * [num_tokens][num_kv_heads][head_dim] bf16, 16-byte aligned; slot_mapping
+ * [num_tokens] int32, -1 skips a token).
+ *
+ * The results are those of the two calls made one after the other. The
+ * difference is the overlap: the library knows what the write touches, so
+ * the decode grid of a batch of one-query (or at most 32/G-query) requests
+ * reads its inputs and the keys before each request's first query position
+ * while the write is still running, and waits for the write only before the
+ * keys from that position on. It therefore REQUIRES that slot_mapping[t] be
+ * the pool slot that block_table gives to token t's position
+ * (seq_len - query_len + j for the request's query j): the slots the step
+ * appends. A slot outside the pool sets PKV_DEV_BAD_SLOT as in
+ * pkv_kv_cache_write; a slot elsewhere in the pool gives unspecified results
+ * (the debug mode, PKV_DEBUG_CHECKS=1 in the Python binding, checks the
+ * mapping). Batches with prefill chunks, and batches of several-query
+ * requests that run longest context first, wait for the write as the
+ * separate calls do.
+ *
+ * Errors: as the two calls; every check of both runs before anything is
+ * enqueued.
+ */
+pkv_status pkv_paged_attention_varlen_append(
+    float *out, float *out_lse, const void *q, void *kv_pool, const void *k_new,
+    const void *v_new, const int32_t *slot_mapping, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+    int32_t num_seqs, int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float scale, int32_t partition_size, void *workspace,
+    size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * pkv_paged_attention_varlen_range -- the same attention over a range of
  * each request's keys, for work split along the sequence: sequence
  * parallelism, where each GPU holds part of a long context, or any caller

@@ -34,6 +34,9 @@ _SIGNATURES = {
     "pkv_paged_attention_varlen": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
+    "pkv_paged_attention_varlen_append": (
+        _i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp] + [_i32] * 9
+        + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
     "pkv_paged_attention_varlen_range": (
         _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp] + [_i32] * 9
         + [ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp, _vp]),
@@ -208,6 +211,67 @@ def paged_attention_varlen(q: torch.Tensor, kv_pool: torch.Tensor, block_table: 
         int(max_seq_len), h, hkv, d, bs, nb, float(scale), int(partition_size),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, q.device))
     _check(st, "paged_attention_varlen")
+    return out, out_lse
+
+
+def paged_attention_varlen_append(q: torch.Tensor, kv_pool: torch.Tensor, k_new: torch.Tensor,
+                                  v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                                  block_table: torch.Tensor, cu_seqlens: torch.Tensor,
+                                  seq_lens: torch.Tensor, max_query_len: int, max_seq_len: int, *,
+                                  out: torch.Tensor | None = None,
+                                  out_lse: torch.Tensor | None = None, scale: float | None = None,
+                                  partition_size: int = -1, workspace: torch.Tensor | None = None,
+                                  dev_status: torch.Tensor | None = None, stream=None):
+    """A step's KV write and attention in one call (``kv_cache_write`` then
+    ``paged_attention_varlen``, overlapped). ``slot_mapping[t]`` must be the
+    pool slot ``block_table`` gives to token t's position (the step's
+    appended slots). Returns ``(out, out_lse)`` as ``paged_attention_varlen``."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(kv_pool, torch.bfloat16, 5, "kv_pool")
+    _need(k_new, torch.bfloat16, 3, "k_new")
+    _need(v_new, torch.bfloat16, 3, "v_new")
+    _need(slot_mapping, torch.int32, 1, "slot_mapping")
+    _need(block_table, torch.int32, 2, "block_table")
+    _need(cu_seqlens, torch.int32, 1, "cu_seqlens")
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    t, h, d = q.shape
+    _, nb, bs, hkv, d2 = kv_pool.shape
+    if d2 != d:
+        raise ValueError("q and kv_pool head_dim differ")
+    if slot_mapping.shape[0] != t or tuple(k_new.shape) != (t, hkv, d) or \
+            tuple(v_new.shape) != (t, hkv, d):
+        raise ValueError("k_new / v_new must be [num_tokens, num_kv_heads, head_dim] and "
+                         "slot_mapping [num_tokens]")
+    b = seq_lens.shape[0]
+    if cu_seqlens.shape[0] != b + 1 or block_table.shape[0] != b:
+        raise ValueError("cu_seqlens must be [B+1] and block_table [B, max_blocks]")
+    if out is None:
+        out = torch.empty((t, h, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, 3, "out")
+    if out_lse is not None:
+        _need(out_lse, torch.float32, 2, "out_lse")
+    if dev_status is not None:
+        _need(dev_status, torch.int32, 1, "dev_status")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if debug_checks.enabled():
+        debug_checks.check_slot_mapping(slot_mapping, num_blocks=nb, block_size=bs)
+        debug_checks.check_attention_tables(
+            cu_seqlens, seq_lens, block_table, num_tokens=t, max_query_len=int(max_query_len),
+            max_seq_len=int(max_seq_len), num_blocks=nb, block_size=bs)
+        debug_checks.check_append_slots(cu_seqlens, seq_lens, block_table, slot_mapping,
+                                        block_size=bs)
+    need = attention_workspace_size(b, t, h, hkv, d, max_seq_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().pkv_paged_attention_varlen_append(
+        _ptr(out), _ptr(out_lse), _ptr(q), _ptr(kv_pool), _ptr(k_new), _ptr(v_new),
+        _ptr(slot_mapping), _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens),
+        _ptr(seq_lens), b, t, int(max_query_len), int(max_seq_len), h, hkv, d, bs, nb,
+        float(scale), int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status),
+        _stream(stream, q.device))
+    _check(st, "paged_attention_varlen_append")
     return out, out_lse
 
 

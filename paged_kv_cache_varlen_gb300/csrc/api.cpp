@@ -472,6 +472,39 @@ pkv_status pkv_paged_attention_varlen(float* out, float* out_lse, const void* q,
   return launch_plan(a, static_cast<cudaStream_t>(stream));
 }
 
+pkv_status pkv_paged_attention_varlen_append(
+    float* out, float* out_lse, const void* q, void* kv_pool, const void* k_new, const void* v_new,
+    const int32_t* slot_mapping, const int32_t* block_table, int32_t max_blocks_per_seq,
+    const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_seqs, int32_t num_tokens,
+    int32_t max_query_len, int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, int32_t partition_size,
+    void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  // every check of both parts before the first launch
+  AttnPlan a;
+  pkv_status s = plan_attention(&a, out, out_lse, q, kv_pool, block_table, max_blocks_per_seq,
+                                cu_seqlens_q, seq_lens, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, partition_size, nullptr, nullptr, dev_status);
+  if (s != PKV_OK || a.empty) return s;
+  if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_INVALID_ARG;
+  if ((s = bind_workspace(&a, workspace, workspace_bytes)) != PKV_OK) return s;
+  if ((s = encode_plan(&a)) != PKV_OK) return s;
+  pkv::KvWriteParams w;
+  w.pool = kv_pool;
+  w.k_new = k_new;
+  w.v_new = v_new;
+  w.slot_mapping = slot_mapping;
+  w.num_tokens = num_tokens;
+  w.num_slots = (int64_t)num_blocks * block_size;
+  w.row_vecs = num_kv_heads * head_dim / 8;
+  w.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pkv::launch_kv_write(w, st) != cudaSuccess) return PKV_ERR_CUDA;
+  a.p.early_pool = 1;
+  return launch_plan(a, st);
+}
+
 pkv_status pkv_paged_attention_varlen_range(
     float* out, float* out_lse, const void* q, const void* kv_pool, const int32_t* block_table,
     int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q, const int32_t* seq_lens,

@@ -105,10 +105,16 @@ __device__ __forceinline__ uint32_t swz(int token, int unit) {
 }
 
 // UNITQ: one query per request, request i being query i (no cu_seqlens
-// array is read). ORDERED: grid slice z takes request p.order[z]. Separate
+// array is read). ORDERED: grid slice z takes request p.order[z]. EARLY: the
+// grid before this one is the call's own KV write, which let this grid
+// launch only once everything before it had completed; it writes only the
+// slots of the requests' query positions, so a CTA reads its inputs and the
+// keys before its first query's position without waiting for it, and waits
+// (the issuing lane of each warp) only before the copy of a chunk that holds
+// a query position, and (every thread) before its output stores. Separate
 // instantiations, so that every prologue's loads stay branch-free (a
 // run-time choice there cost up to 5 %).
-template <int D, int SPW, int MINB, bool UNITQ, bool ORDERED>
+template <int D, int SPW, int MINB, bool UNITQ, bool ORDERED, bool EARLY>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
   constexpr int KS = D / 16;            // k-steps of QK^T
@@ -132,8 +138,9 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       return;
     }
   } else {
-    // Everything below may read the pool the preceding KV write produces.
-    griddep_wait();
+    // Everything below may read the pool the preceding KV write produces
+    // (EARLY: see above).
+    if constexpr (!EARLY) griddep_wait();
     griddep_launch_dependents();
   }
 
@@ -210,6 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   __syncwarp();
 
   const int32_t nrows = p.num_blocks * p.block_size;
+  bool waited = false;  // EARLY: this lane has waited for the KV write
   auto issue = [&](int k, int32_t id) {  // lane 0 only
     const int slot = k % SPW;
     const uint32_t bar = smem_addr(&bars[warp * SPW + slot]);
@@ -220,6 +228,12 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     }
     const uint32_t dst = smem_addr(slots + (warp * SPW + slot) * SLOT);
     const int key0 = kbeg + (warp + k * kWarps) * kChunk;
+    if constexpr (EARLY) {
+      if (!waited && key0 + kChunk > qpos0) {  // the chunk holds a query position
+        griddep_wait();
+        waited = true;
+      }
+    }
     const int32_t row = id * p.block_size + key0 % p.block_size;
     mbar_arrive_expect_tx(bar, SLOT);
     tma_load_4d(dst, &kv_map, bar, 0, row, kvh, 0);
@@ -412,6 +426,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   l1 += __shfl_xor_sync(kFull, l1, 2);
 
   __syncthreads();  // every warp is done with its slots: reuse them
+  if constexpr (EARLY) griddep_wait();  // before the first output store
   // rows padded to D + 8 floats: the quads of 4 consecutive rows store to
   // disjoint banks; rows past the CTA's own are not stored at all
   constexpr int RS = D + 8;
@@ -609,11 +624,16 @@ cudaError_t launch_decode_mma_d(const AttnParams& p, const CUtensorMap& kv_map,
   const size_t smem = 1024 + kWarps * SPW * SLOT + kWarps * SPW * sizeof(uint64_t) + 16;
   const bool unitq = p.cu_seqlens == nullptr;
   const bool ordered = p.order != nullptr && !unitq && !p.after_prefill && p.num_seqs <= 256;
-  auto kernel = unitq     ? decode_mma_kernel<D, SPW, MINB, true, false>
-                : ordered ? decode_mma_kernel<D, SPW, MINB, false, true>
-                          : decode_mma_kernel<D, SPW, MINB, false, false>;
-  static SmemLimit limit_cu, limit_unit, limit_ordered;
-  SmemLimit& limit = unitq ? limit_unit : ordered ? limit_ordered : limit_cu;
+  const bool early = p.early_pool && !unitq && !ordered && !p.after_prefill && !p.key_start;
+  auto kernel = unitq     ? decode_mma_kernel<D, SPW, MINB, true, false, false>
+                : ordered ? decode_mma_kernel<D, SPW, MINB, false, true, false>
+                : early   ? decode_mma_kernel<D, SPW, MINB, false, false, true>
+                          : decode_mma_kernel<D, SPW, MINB, false, false, false>;
+  static SmemLimit limit_cu, limit_unit, limit_ordered, limit_early;
+  SmemLimit& limit = unitq     ? limit_unit
+                     : ordered ? limit_ordered
+                     : early   ? limit_early
+                               : limit_cu;
   if (cudaError_t e = limit.ensure(reinterpret_cast<const void*>(kernel), (int)smem);
       e != cudaSuccess)
     return e;

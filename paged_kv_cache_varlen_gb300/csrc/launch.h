@@ -118,6 +118,11 @@ struct AttnParams {
   // by a one-CTA kernel launched before the decode grid (longest context
   // first)
   int32_t* order;
+  // decode grid only: the kernel enqueued right before it is this call's own
+  // KV write (pkv_paged_attention_varlen_append), which writes only the slots
+  // of the requests' query positions: CTAs of a plain decode batch read the
+  // keys before the first query's position without waiting for it
+  int32_t early_pool;
 };
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);

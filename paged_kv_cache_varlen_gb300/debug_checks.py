@@ -92,6 +92,26 @@ def check_attention_tables(cu_seqlens, seq_lens, block_table, *, num_tokens: int
                              f"[0, {num_blocks})")
 
 
+def check_append_slots(cu_seqlens, seq_lens, block_table, slot_mapping, *,
+                       block_size: int) -> None:
+    """For the combined KV write and attention call: raise ValueError unless
+    every token's slot (-1: skipped) is the pool slot block_table gives to the
+    token's position, seq_len - query_len + j for its request's query j."""
+    cu = _host(cu_seqlens).astype(np.int64)
+    lens = _host(seq_lens).astype(np.int64)
+    table = _host(block_table).astype(np.int64)
+    slots = _host(slot_mapping).astype(np.int64)
+    qlen = np.diff(cu)
+    req = np.repeat(np.arange(lens.shape[0]), qlen)
+    pos = lens[req] - qlen[req] + (np.arange(cu[-1]) - cu[req])
+    want = table[req, pos // block_size] * block_size + pos % block_size
+    bad = np.nonzero((slots != -1) & (slots != want))[0]
+    if bad.size:
+        t = int(bad[0])
+        raise ValueError(f"slot_mapping[{t}] = {slots[t]}: request {int(req[t])}'s position "
+                         f"{int(pos[t])} is slot {int(want[t])}")
+
+
 def check_slot_mapping(slot_mapping, *, num_blocks: int, block_size: int) -> None:
     """Raise ValueError on the first slot outside the pool (-1 is skipped)."""
     slots = _host(slot_mapping).astype(np.int64)

@@ -121,6 +121,32 @@ def test_partition_count_limit(lib):
     assert lib.pkv_attention_workspace_size(1, 1, 4, 2, 128, over, 16) == 0
 
 
+def _append(lib, **over):
+    args = dict(out=16, out_lse=None, q=16, kv_pool=16, k_new=16, v_new=16, slot_mapping=16,
+                block_table=16, max_blocks=4, cu=16, seq_lens=16, num_seqs=1, num_tokens=1,
+                max_query_len=1, max_seq_len=16, num_heads=4, num_kv_heads=2, head_dim=128,
+                block_size=16, num_blocks=4, scale=0.125, partition_size=-1, workspace=None,
+                workspace_bytes=0, dev_status=None, stream=None)
+    args.update(over)
+    return lib.pkv_paged_attention_varlen_append(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"k_new": None}, 1),
+    ({"slot_mapping": None}, 1),
+    ({"v_new": 24}, 1),                  # not 16-byte aligned
+    ({"q": None}, 1),                    # the attention's own checks, before the write
+    ({"head_dim": 96}, 2),
+    ({}, 4),                             # every argument valid: stops at the missing workspace
+])
+def test_append_rejects_before_launch(lib, over, status):
+    assert _append(lib, **over) == status
+
+
+def test_append_empty_batch_is_a_no_op(lib):
+    assert _append(lib, num_tokens=0, out=None, q=None, k_new=None) == 0
+
+
 def test_empty_batch_is_a_no_op(lib):
     assert _attn(lib, num_tokens=0, out=None, q=None) == 0
 

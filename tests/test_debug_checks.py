@@ -100,3 +100,21 @@ def test_switch(monkeypatch):
     assert not dc.enabled()
     monkeypatch.setenv("PKV_DEBUG_CHECKS", "1")
     assert dc.enabled()
+
+
+@pytest.mark.parametrize("name", ["tiny", "spec_verify", "mixed_step"])
+def test_append_slots_of_valid_steps_pass(name):
+    w = wl.CONFIGS[name](poison=False)
+    dc.check_append_slots(w.cu_seqlens, w.seq_lens, w.block_table, w.slot_mapping,
+                          block_size=w.block_size)
+
+
+def test_append_slot_elsewhere_in_the_pool(small):
+    w = small
+    s = w.slot_mapping.copy()
+    s[1] = -1                    # a skipped token is allowed
+    dc.check_append_slots(w.cu_seqlens, w.seq_lens, w.block_table, s, block_size=w.block_size)
+    s[2] = (s[2] + w.block_size) % (w.num_blocks * w.block_size)   # another block's slot
+    with pytest.raises(ValueError, match=r"slot_mapping\[2\]"):
+        dc.check_append_slots(w.cu_seqlens, w.seq_lens, w.block_table, s,
+                              block_size=w.block_size)
