@@ -14,7 +14,9 @@ cu_seqlens_q non-decreasing from 0 to num_tokens; every request's query count
 at most max_query_len; its context length at least its query count (or, for
 key ranges, at least 1 with non-negative positions), at most max_seq_len and
 within its table row; every block id a request's context covers inside the
-pool; every slot of the KV write inside the pool (or -1, skipped).
+pool; every slot of the KV write inside the pool (or -1, skipped); and, for
+the combined KV write and attention call, every slot the one block_table gives
+to its token's query position.
 """
 from __future__ import annotations
 
