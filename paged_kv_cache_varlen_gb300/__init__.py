@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     library_path,
     lse_merge,
     paged_attention_varlen,
+    paged_attention_varlen_append,
     paged_attention_varlen_range,
 )
 
@@ -22,5 +23,6 @@ __all__ = [
     "library_path",
     "lse_merge",
     "paged_attention_varlen",
+    "paged_attention_varlen_append",
     "paged_attention_varlen_range",
 ]
